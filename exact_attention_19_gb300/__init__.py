@@ -1,0 +1,129 @@
+"""GB300-native fused exact-attention forward (sm_103a).
+
+Thin ctypes binding over ``libfa_gb300.so`` (C ABI in ``include/fa.h``):
+argument marshalling only, every step of the computation runs in the CUDA
+kernel.  PyTorch supplies device memory and streams.
+
+    o, lse = fwd(q, k, v, causal=False)          # torch bf16 [B, H, N, d]
+    fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, causal, stream)
+
+There is no fallback: if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+__all__ = ["FaError", "fa_fwd", "fa_strerror", "fa_version", "fa_fwd_status", "fwd", "library_path",
+           "load", "STATUS"]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libfa_gb300.so")
+
+STATUS = {
+    0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_ALIGN", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
+    5: "FA_ERR_CAUSAL_SHAPE", 6: "FA_ERR_LAUNCH", 7: "FA_ERR_DEVICE", 8: "FA_ERR_TIMEOUT",
+    9: "FA_ERR_SCALE", 10: "FA_ERR_POINTER",
+}
+
+_lib = None
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, where: str = "fa_fwd"):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({fa_strerror(status)})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libfa_gb300.so (built by ``build.py`` / ``__graft_entry__.build``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                              "`python -c 'import __graft_entry__ as g; g.build()'`")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i32 = ctypes.c_void_p, ctypes.c_int
+        lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp]
+        lib.fa_fwd.restype = i32
+        lib.fa_strerror.argtypes = [i32]
+        lib.fa_strerror.restype = ctypes.c_char_p
+        lib.fa_version.argtypes = []
+        lib.fa_version.restype = i32
+        lib.fa_fwd_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint), i32]
+        lib.fa_fwd_status.restype = i32
+        _lib = lib
+    return _lib
+
+
+def fa_strerror(status: int) -> str:
+    return load().fa_strerror(int(status)).decode()
+
+
+def fa_version() -> int:
+    return int(load().fa_version())
+
+
+def fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream) -> int:
+    """Raw C-ABI call with integer device pointers and a raw stream handle.
+
+    Returns the status code (0 = FA_OK); does not raise.
+    """
+    return int(load().fa_fwd(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                             int(causal), stream))
+
+
+def fa_fwd_status(stream=None, clear: bool = False):
+    """(status, raw device status word) after synchronising ``stream``."""
+    word = ctypes.c_uint(0)
+    st = int(load().fa_fwd_status(stream, ctypes.byref(word), int(bool(clear))))
+    return st, int(word.value)
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+    """O = softmax(q k^T * scale) v and the per-row LSE, on the GPU.
+
+    q: [B, H, Nq, d], k, v: [B, H, Nk, d] torch.bfloat16 CUDA tensors,
+    contiguous.  ``scale`` defaults to 1/sqrt(d).  ``out`` (bf16 [B,H,Nq,d])
+    and ``lse`` (fp32 [B,H,Nq]) may be given to avoid allocation.  Runs on
+    ``stream`` (default: the current torch stream), asynchronously.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise TypeError(f"{name} must be a CUDA torch.bfloat16 tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    B, H, Nq, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    Nk = k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d,
+                scale, int(bool(causal)), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st)
+    return out, lse

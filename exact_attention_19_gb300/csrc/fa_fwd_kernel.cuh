@@ -1,0 +1,425 @@
+// fa_fwd_kernel.cuh -- the fused exact-attention forward kernel for sm_103a.
+//
+// Algorithm (FA2 loop order: page "llm-infra-atlas / FlashAttention 01",
+// section 3): one CTA owns query tiles and streams every visible K/V tile
+// past them.  Per K/V tile j and query tile Q_i:
+//   S = Q_i K_j^T                 GEMM-I, tensor cores, fp32 in TMEM
+//   mask (causal diagonal tile, ragged key tail) -> -inf
+//   m_new = max(m, rowmax S)      online softmax, section 2 of the same page
+//   P = 2^(S*c - m_bar)           c = scale * log2(e) (section 4, exp2 form)
+//   l = alpha*l + rowsum P; O = alpha*O + P V_j   (GEMM-II into TMEM)
+// and at the end O / l and LSE = ln 2 * (m_bar + log2 l) (section 3, 5).
+// The reference m_bar moves only when the candidate maximum exceeds it by
+// more than tau = 8 in base-2 units ("conditional softmax rescaling", page
+// "pinghaoyang FlashAttention 1-4 guide", FA4 section); the final division
+// by the true normaliser keeps the result exact.  S and P never leave the SM.
+//
+// GB300 mapping (one CTA per SM, 320 threads):
+//   warps 0-3  softmax + correction + epilogue for query tile 0 (TMEM lanes 0-127)
+//   warps 4-7  the same for query tile 1
+//   warp  8    TMA producer: Q tiles once, K/V tiles through a ring of
+//              `kStages` stages each (mbarrier full/empty pairs)
+//   warp  9    MMA issuer: tcgen05.mma (one thread), commits to mbarriers
+// TMEM (512 columns x 128 lanes x 32 bit):
+//   S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D);
+//   P_i (bf16, packed in pairs) overwrites the first 64 columns of S_i and is
+//   the A operand of GEMM-II straight from TMEM.
+// Shared memory: Q0, Q1, K ring, V ring; each tile 128 rows x D bf16 stored
+// as D/64 boxes of 128 rows x 128 bytes with the 128-byte swizzle that TMA
+// writes and the MMA descriptors read (K-major for Q and K, MN-major for V).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+// Device status word: bit 0 set when any wait gave up; bits 8.. hold the
+// roles that gave up (1 softmax, 2 producer, 4 MMA, 8 epilogue).
+__device__ unsigned int g_fa_status;
+
+struct FwdParams {
+  void* o;            // bf16 [BH, Nq, D]
+  float* lse;         // fp32 [BH, Nq]
+  int Nq, Nk;
+  int n_pairs;        // ceil(Nq / 256): CTAs per (b, h)
+  float scale_log2;   // scale * log2(e)
+};
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kThreads = 320;
+  static constexpr int kBM = 128;  // query rows per tile (MMA M)
+  static constexpr int kBN = 128;  // keys per tile
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kBoxes = D / 64;  // 128-byte swizzle boxes per row
+  static constexpr uint32_t kBoxBytes = 128u * 128u;
+  static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKOff = 2 * kTileBytes;
+  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
+  static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
+  static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // barriers, then alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
+  static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);  // S = Q K^T
+  static constexpr uint32_t kIdescO = idesc_bf16(128, D, true);     // O += P V
+};
+
+// barrier slots (8 bytes each) inside the barrier block
+enum : int { kBarQ = 0, kBarS = 2, kBarP = 4, kBarO = 6, kBarDrain = 8, kBarRing = 9 };
+
+__device__ __forceinline__ void report_wait_failure(volatile int* abort, unsigned role) {
+  *abort = 1;
+  atomicOr(&g_fa_status, 1u | (role << 8));
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const sbase = smem_raw + (base - raw_addr);
+
+  const uint32_t bar0 = base + C::kBarOff;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const int kBarKFull = kBarRing, kBarKEmpty = kBarRing + C::kStages;
+  const int kBarVFull = kBarRing + 2 * C::kStages, kBarVEmpty = kBarRing + 3 * C::kStages;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::kBarOff + 192);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + C::kBarOff + 196);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(kBarQ + 0), 1);
+    mbar_init(bar(kBarQ + 1), 1);
+    mbar_init(bar(kBarS + 0), 1);
+    mbar_init(bar(kBarS + 1), 1);
+    mbar_init(bar(kBarP + 0), 128);
+    mbar_init(bar(kBarP + 1), 128);
+    mbar_init(bar(kBarO + 0), 1);
+    mbar_init(bar(kBarO + 1), 1);
+    mbar_init(bar(kBarDrain), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(bar(kBarKFull + s), 1);
+      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- work item: (b*H + h, pair of query tiles) --------------------------
+  const int bh = blockIdx.x / p.n_pairs;
+  int pair = blockIdx.x % p.n_pairs;
+  if (CAUSAL) pair = p.n_pairs - 1 - pair;  // heaviest pair of each head first
+  const int n_kv_all = (p.Nk + C::kBN - 1) / C::kBN;
+  int row0[2], nkv[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = 2 * pair + t;
+    row0[t] = qt * C::kBM;
+    nkv[t] = (row0[t] < p.Nq) ? (CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all) : 0;
+  }
+  const int n_max = max(nkv[0], nkv[1]);
+
+  if (warp == 8) {
+    // ======================= TMA producer =================================
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      for (int t = 0; t < 2; ++t) {
+        if (nkv[t] == 0) continue;
+        const uint32_t dst = base + C::kQOff + t * C::kTileBytes;
+        mbar_arrive_expect_tx(bar(kBarQ + t), C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(dst + b * C::kBoxBytes, &tmQ, bar(kBarQ + t), b * 64, row0[t], bh);
+      }
+      int issued = 0;  // K/V tiles issued
+      bool failed = false;
+      for (int j = 0; j < n_max; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (!mbar_wait(bar(kBarKEmpty + s), ph ^ 1u, abort_flag)) { failed = true; break; }
+        mbar_arrive_expect_tx(bar(kBarKFull + s), C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(base + C::kKOff + s * C::kTileBytes + b * C::kBoxBytes, &tmK, bar(kBarKFull + s),
+                      b * 64, j * C::kBN, bh);
+        if (!mbar_wait(bar(kBarVEmpty + s), ph ^ 1u, abort_flag)) {
+          failed = true;
+          issued = -(j + 1);  // K of tile j issued, V not
+          break;
+        }
+        mbar_arrive_expect_tx(bar(kBarVFull + s), C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(base + C::kVOff + s * C::kTileBytes + b * C::kBoxBytes, &tmV, bar(kBarVFull + s),
+                      b * 64, j * C::kBN, bh);
+        issued = j + 1;
+      }
+      if (failed) {
+        report_wait_failure(abort_flag, 2u);
+      }
+      if (*abort_flag) {
+        // Let every copy already issued land before the CTA can exit.
+        const int nk = issued >= 0 ? issued : -issued;
+        const int nv = issued >= 0 ? issued : -issued - 1;
+        for (int s = 0; s < C::kStages; ++s) {
+          int jk = -1, jv = -1;
+          for (int j = 0; j < nk; ++j)
+            if (j % C::kStages == s) jk = j;
+          for (int j = 0; j < nv; ++j)
+            if (j % C::kStages == s) jv = j;
+          if (jk >= 0) mbar_wait(bar(kBarKFull + s), (jk / C::kStages) & 1, nullptr);
+          if (jv >= 0) mbar_wait(bar(kBarVFull + s), (jv / C::kStages) & 1, nullptr);
+        }
+        for (int t = 0; t < 2; ++t)
+          if (nkv[t] > 0) mbar_wait(bar(kBarQ + t), 0, nullptr);
+      }
+    }
+  } else if (warp == 9) {
+    // ======================= MMA issuer ====================================
+    if (lane == 0) {
+      const uint32_t sQ[2] = {base + C::kQOff, base + C::kQOff + C::kTileBytes};
+      const uint32_t tS[2] = {tmem + C::kTmS0, tmem + C::kTmS1};
+      const uint32_t tO[2] = {tmem + C::kTmO0, tmem + C::kTmO1};
+      // GEMM-I: S_t = Q_t K^T over D/16 k-steps of 16 (K-major, 128B swizzle:
+      // k-step kk lives in box kk/4 at byte offset 32*(kk%4) of each row).
+      auto gemm1 = [&](int t, int s) {
+        const uint32_t sK = base + C::kKOff + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
+          mma_ss(tS[t], sdesc_sw128(sQ[t] + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), C::kIdescS,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      // GEMM-II: O_t += P_t V over 128/16 k-steps; P_t from TMEM (8 columns of
+      // packed bf16 pairs per step), V MN-major: 16 keys = 2048 bytes per step,
+      // second 64-column box of V at LBO = one box.
+      auto gemm2 = [&](int t, int s, bool acc_prev) {
+        const uint32_t sV = base + C::kVOff + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < C::kBN / 16; ++kk) {
+          mma_ts(tO[t], tS[t] + kk * 8, sdesc_sw128(sV + kk * 2048, C::kBoxBytes, 1024), C::kIdescO,
+                 (acc_prev || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t)
+        if (nkv[t] > 0) ok = mbar_wait(bar(kBarQ + t), 0, abort_flag);
+      if (ok && n_max > 0) ok = mbar_wait(bar(kBarKFull + 0), 0, abort_flag);
+      if (ok && n_max > 0) {
+        tc_fence_after();
+        for (int t = 0; t < 2; ++t)
+          if (nkv[t] > 0) {
+            gemm1(t, 0);
+            mma_commit(bar(kBarS + t));
+          }
+        mma_commit(bar(kBarKEmpty + 0));
+      }
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int sv = j % C::kStages;
+        const bool has_next = (j + 1) < n_max;
+        const int sk = (j + 1) % C::kStages;
+        if (!(ok = mbar_wait(bar(kBarVFull + sv), (j / C::kStages) & 1, abort_flag))) break;
+        tc_fence_after();
+        if (j < nkv[0]) {
+          if (!(ok = mbar_wait(bar(kBarP + 0), j & 1, abort_flag))) break;
+          tc_fence_after();
+          gemm2(0, sv, j > 0);
+          if (j == nkv[0] - 1) mma_commit(bar(kBarO + 0));
+        }
+        if (has_next) {
+          if (!(ok = mbar_wait(bar(kBarKFull + sk), ((j + 1) / C::kStages) & 1, abort_flag))) break;
+          tc_fence_after();
+        }
+        if (j + 1 < nkv[0]) {
+          gemm1(0, sk);
+          mma_commit(bar(kBarS + 0));
+        }
+        if (j < nkv[1]) {
+          if (!(ok = mbar_wait(bar(kBarP + 1), j & 1, abort_flag))) break;
+          tc_fence_after();
+          gemm2(1, sv, j > 0);
+          if (j == nkv[1] - 1) mma_commit(bar(kBarO + 1));
+        }
+        mma_commit(bar(kBarVEmpty + sv));
+        if (j + 1 < nkv[1]) {
+          gemm1(1, sk);
+          mma_commit(bar(kBarS + 1));
+        }
+        if (has_next) mma_commit(bar(kBarKEmpty + sk));
+      }
+      if (!ok) report_wait_failure(abort_flag, 4u);
+      // Drain: every MMA issued so far has completed once this barrier flips.
+      mma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, nullptr);
+    }
+  } else {
+    // ============== softmax / correction / epilogue (warps 0-7) ===========
+    const int t = warp >> 2;        // query tile of this warpgroup
+    const int wq = warp & 3;        // TMEM lane quarter
+    const int row_local = wq * 32 + lane;
+    const int row = row0[t] + row_local;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tS = lane_base + (t == 0 ? C::kTmS0 : C::kTmS1);
+    const uint32_t tO = lane_base + (t == 0 ? C::kTmO0 : C::kTmO1);
+    const float c = p.scale_log2;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    float m_bar = NEG_INF;  // reference maximum, base-2 scaled units
+    float l = 0.f;
+    bool ok = true;
+    const int nt = nkv[t];
+    for (int j = 0; j < nt; ++j) {
+      bool got = mbar_wait(bar(kBarS + t), j & 1, abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) { ok = false; break; }
+      tc_fence_after();
+      uint32_t s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32(tS + 0, s0);
+      tmem_ld32(tS + 32, s1);
+      tmem_ld32(tS + 64, s2);
+      tmem_ld32(tS + 96, s3);
+      tmem_ld_wait(s0);
+      reg_pin(s1);
+      reg_pin(s2);
+      reg_pin(s3);
+      float* const f0 = reinterpret_cast<float*>(s0);
+      float* const f1 = reinterpret_cast<float*>(s1);
+      float* const f2 = reinterpret_cast<float*>(s2);
+      float* const f3 = reinterpret_cast<float*>(s3);
+
+      // masking: ragged key tail and the causal diagonal tile
+      const bool tail = (j == n_kv_all - 1) && (p.Nk % C::kBN != 0);
+      const bool diag = CAUSAL && (j == nt - 1);
+      if (tail || diag) {
+        int lim = p.Nk;
+        if (CAUSAL) lim = min(lim, row + 1);
+        lim -= j * C::kBN;  // columns >= lim are masked
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (i >= lim) f0[i] = NEG_INF;
+          if (32 + i >= lim) f1[i] = NEG_INF;
+          if (64 + i >= lim) f2[i] = NEG_INF;
+          if (96 + i >= lim) f3[i] = NEG_INF;
+        }
+      }
+      float mx0 = f0[0], mx1 = f1[0], mx2 = f2[0], mx3 = f3[0];
+#pragma unroll
+      for (int i = 1; i < 32; ++i) {
+        mx0 = fmaxf(mx0, f0[i]);
+        mx1 = fmaxf(mx1, f1[i]);
+        mx2 = fmaxf(mx2, f2[i]);
+        mx3 = fmaxf(mx3, f3[i]);
+      }
+      const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+      const bool need = m_new > m_bar + 8.0f;
+      const bool any_need = __any_sync(0xffffffffu, need);
+      float alpha = 1.0f;
+      if (need) {
+        alpha = ex2(m_bar - m_new);  // 0 on the first visible tile (m_bar = -inf)
+        m_bar = m_new;
+        l *= alpha;
+      }
+      const float m_ref = (m_bar == NEG_INF) ? 0.f : m_bar;
+      // P = 2^(S*c - m_ref), rounded to bf16 pairs into the first 64 columns
+      // of this tile's S region (16 columns = 32 probabilities per store).
+      float ls0 = 0.f, ls1 = 0.f;
+      auto emit = [&](const float* f, uint32_t col) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float e0 = ex2(fmaf(f[2 * i], c, -m_ref));
+          const float e1 = ex2(fmaf(f[2 * i + 1], c, -m_ref));
+          ls0 += e0;
+          ls1 += e1;
+          pk[i] = pack_bf16(e0, e1);
+        }
+        tmem_st16(tS + col, pk);
+      };
+      emit(f0, 0);
+      emit(f1, 16);
+      emit(f2, 32);
+      emit(f3, 48);
+      l += ls0 + ls1;
+      // correction: O *= alpha for the rows whose reference moved (the
+      // previous P V of this tile has completed: S of this tile was issued
+      // after it and its commit covers it).
+      if (any_need && j > 0) {
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + cc * 32, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarP + t));
+    }
+    if (!ok) report_wait_failure(abort_flag, 1u);
+    if (ok && nt > 0) {
+      bool got = mbar_wait(bar(kBarO + t), 0, abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        report_wait_failure(abort_flag, 8u);
+      } else {
+        tc_fence_after();
+        const float inv_l = (l > 0.f) ? (1.0f / l) : 0.f;
+        const bool store = row < p.Nq;
+        uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                     (static_cast<size_t>(bh) * p.Nq + row) * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + cc * 32, o);
+          tmem_ld_wait(o);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (store) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              orow[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+        if (store) {
+          const float lse = (l > 0.f) ? (m_bar + __log2f(l)) * 0.69314718055994530942f : NEG_INF;
+          p.lse[static_cast<size_t>(bh) * p.Nq + row] = lse;
+        }
+      }
+    }
+  }
+
+  // ---- teardown -----------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -1,0 +1,96 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) fused exact-attention forward library
+ *         libfa_gb300.so.
+ *
+ * The operation (fa_fwd) is the tiled exact-attention forward pass:
+ *
+ *   O   = softmax(Q K^T * scale) V          per (batch, head), row-wise softmax
+ *   LSE = log(sum_j exp(scale * q_i . k_j)) per query row (natural log)
+ *
+ * as defined on the pages "llm-infra-atlas / FlashAttention 01: IO awareness
+ * and online softmax" (section 1 for the three-operation definition, section 3
+ * for the tiled forward loop that emits O and LSE = m + log l, section 5 for
+ * LSE's role in the backward pass) and "lumenova research-attention"
+ * (section 01 for the shapes, section 03 for the per-row recurrence).  The
+ * optional causal mask keeps key j for query row i iff j <= i.
+ *
+ * All functions have C linkage, never throw, never print and never abort the
+ * process.  None of them allocates device memory.
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_NULL = 1,          /* a required pointer is NULL                                  */
+  FA_ERR_ALIGN = 2,         /* a tensor base pointer is not 16-byte aligned                */
+  FA_ERR_SHAPE = 3,         /* B, H, Nk <= 0, a negative Nq, or a size beyond the limits   */
+  FA_ERR_HEADDIM = 4,       /* d is not 64 or 128                                          */
+  FA_ERR_CAUSAL_SHAPE = 5,  /* causal = 1 with Nq != Nk                                    */
+  FA_ERR_LAUNCH = 6,        /* the CUDA runtime refused the launch or a set-up call        */
+  FA_ERR_DEVICE = 7,        /* the current device is not compute capability 10.3 (GB300)  */
+  FA_ERR_TIMEOUT = 8,       /* a kernel wait gave up (reported by fa_fwd_status)           */
+  FA_ERR_SCALE = 9,         /* scale is not a finite positive number                       */
+  FA_ERR_POINTER = 10       /* a tensor pointer is not device memory of the current device */
+} fa_status;
+
+/*
+ * fa_fwd -- fused attention forward on `stream` (asynchronous; no host sync).
+ *
+ * q    [B, H, Nq, d] bf16, contiguous row-major (d fastest), device memory.
+ * k, v [B, H, Nk, d] bf16, contiguous, device memory.
+ * o    [B, H, Nq, d] bf16 output, contiguous, device memory; must not overlap
+ *      q, k, v or lse.
+ * lse  [B, H, Nq] fp32 output: natural-log log-sum-exp of the scaled logits of
+ *      each query row (so that P = exp(scale * q.k - LSE)).
+ * d    head dimension, 64 or 128.
+ * scale  multiplies q.k before the softmax (1/sqrt(d) for standard attention);
+ *        must be finite and > 0.
+ * causal 0: every key is visible; 1: key j is visible to row i iff j <= i
+ *        (requires Nq == Nk).
+ *
+ * Arithmetic: bf16 products accumulated in fp32 on the tensor cores, softmax
+ * in fp32 (base-2 exponentials with log2(e) folded into the scale), the
+ * probabilities rounded to bf16 for the P.V product, fp32 accumulation of O,
+ * one division by the row sum at the end, O rounded to bf16 (nearest even).
+ *
+ * Ownership: the caller owns all five buffers; the library keeps no pointer
+ * after the call returns and allocates nothing.
+ * Errors: argument problems return a code before anything is launched and
+ * nothing is written.  Nq == 0 is a successful no-op; q, o and lse may then be
+ * NULL (k and v may not).  FA_ERR_LAUNCH is
+ * returned if the launch itself fails; faults during execution surface, as
+ * usual for CUDA, at the next synchronising call on the stream.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+           int Nk, int d, float scale, int causal, cudaStream_t stream);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* fa_strerror(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fa_version(void);
+
+/*
+ * fa_fwd_status -- synchronise `stream`, then report whether any fa_fwd kernel
+ * on the current device gave up on a wait (FA_ERR_TIMEOUT) since the last
+ * clear.  Every wait inside the kernel is bounded (about 2 s); a wait that
+ * runs out records the failing role in the device status word, the CTA drains
+ * its in-flight copies and MMAs, frees its tensor memory and exits.  *detail
+ * (optional) receives the raw status word.  clear != 0 resets the word.
+ * Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_LAUNCH if synchronisation failed.
+ */
+int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

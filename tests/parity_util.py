@@ -1,0 +1,66 @@
+"""Helpers shared by the GPU parity tests: upload bf16 bits, run the CUDA path
+through the C ABI binding, compare with the fp64 oracle.
+
+Tolerances (the stated bar, with the readings noted):
+  O:   |O_gpu - O_ref| <= 1e-2 * max(1, |O_ref|) elementwise.  Absolute 1e-2
+       at unit scale; relative above it, since a bf16 output holds only 8
+       significant bits (half an ulp exceeds 1e-2 once |O| >= 4).
+  LSE: |LSE_gpu - LSE_ref| <= 1e-3 * max(1, |LSE_ref|).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+def to_device(bits, device="cuda"):
+    import torch
+
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def run_gpu(q, k, v, scale, causal):
+    """q, k, v: uint16 bf16 bits [B,H,N,d].  Returns (o float64 numpy, lse float64 numpy)."""
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    tq, tk, tv = to_device(q), to_device(k), to_device(v)
+    o, lse = fa.fwd(tq, tk, tv, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    st, word = fa.fa_fwd_status(None, clear=True)
+    assert st == 0, f"kernel wait timed out, status word {word:#x}"
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def o_err(o_gpu, o_ref):
+    return float(np.max(np.abs(o_gpu - o_ref) / np.maximum(1.0, np.abs(o_ref)))) if o_ref.size else 0.0
+
+
+def lse_err(l_gpu, l_ref):
+    return float(np.max(np.abs(l_gpu - l_ref) / np.maximum(1.0, np.abs(l_ref)))) if l_ref.size else 0.0
+
+
+def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    assert np.all(np.isfinite(o_gpu)), f"{what}: non-finite O"
+    assert np.all(np.isfinite(lse_gpu)), f"{what}: non-finite LSE"
+    eo, el = o_err(o_gpu, o_ref), lse_err(lse_gpu, lse_ref)
+    assert eo <= O_TOL, f"{what}: O error {eo:.3e} (max abs {np.max(np.abs(o_gpu - o_ref)):.3e})"
+    assert el <= LSE_TOL, f"{what}: LSE error {el:.3e}"
+    return eo, el
+
+
+def sample_rows(B, H, Nq, n, seed):
+    """Flat row indices: first and last rows of the first and last heads,
+    the tile boundaries around row 128/256 of one head, plus n random rows."""
+    rng = np.random.default_rng(seed)
+    BH = B * H
+    picks = set()
+    for bh in {0, BH - 1, BH // 2}:
+        for i in (0, 1, 2, 127, 128, 129, 255, 256, Nq // 2, Nq - 3, Nq - 2, Nq - 1):
+            if 0 <= i < Nq:
+                picks.add(bh * Nq + i)
+    picks.update(int(x) for x in rng.integers(0, BH * Nq, size=n))
+    return np.array(sorted(picks), dtype=np.int64)

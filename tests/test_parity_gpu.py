@@ -1,0 +1,198 @@
+"""CUDA path vs the fp64 oracle on the same seeded bf16 inputs (GB300 only).
+
+Every call goes through the C ABI (libfa_gb300.so via the ctypes binding).
+Element-wise at sizes the oracle finishes in seconds (several tiles, ragged
+tails); sampled rows at the full benchmark sizes in the launch configuration
+the bench times.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity_util import assert_close, run_gpu, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_19_gb300 as fa
+    from exact_attention_19_gb300 import build
+
+    build.build()
+    fa.load()
+    yield
+
+
+def _check_full(w: synth.Workload):
+    q, k, v = w.make()
+    o, lse = run_gpu(q, k, v, w.scale, w.causal)
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.scale, w.causal)
+    return assert_close(o, lse, o_ref, lse_ref, w.name)
+
+
+# --- the three small workloads, every element ---------------------------------
+@pytest.mark.parametrize("name", ["single_head_256_d64", "single_head_4096_d64", "gpt2_small_causal_1024_d64"])
+def test_workload_elementwise(name):
+    _check_full(synth.WORKLOADS[name])
+
+
+# --- ragged and odd shapes, every element --------------------------------------
+RAGGED = [1, 2, 63, 65, 127, 129, 255, 257, 383, 1000]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", RAGGED)
+def test_ragged_square(n, d, causal):
+    _check_full(synth.Workload(f"ragged{n}", 1, 2, n, n, d, causal, seed=500 + n))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("nq,nk", [(100, 300), (513, 64), (1, 1000), (256, 129), (700, 4097)])
+def test_rectangular_noncausal(nq, nk, d):
+    _check_full(synth.Workload(f"rect{nq}x{nk}", 2, 1, nq, nk, d, False, seed=900 + nq))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_multi_batch_head(d):
+    _check_full(synth.Workload("bh", 3, 5, 200, 200, d, True, seed=31))
+    _check_full(synth.Workload("bh", 2, 7, 130, 390, d, False, seed=32))
+
+
+# --- degenerate and numerically hard cases -----------------------------------
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_key(d):
+    w = synth.Workload("nk1", 1, 3, 300, 1, d, False, seed=3)
+    q, k, v = w.make()
+    o, lse = run_gpu(q, k, v, w.scale, False)
+    # closed form: O = V[0] exactly (bf16 V reproduced exactly), LSE = scale * q.k0
+    vv = synth.bf16_to_f32(v).astype(np.float64)
+    assert np.array_equal(o, np.broadcast_to(vv[:, :, :1, :], o.shape))
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.scale, False)
+    assert_close(o, lse, o_ref, lse_ref, "nk1")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_keys_give_uniform_weights(causal):
+    n, d = 300, 128
+    q = synth.normal_bf16(4, 0, (1, 1, n, d))
+    k = np.zeros((1, 1, n, d), dtype=np.uint16)
+    v = synth.normal_bf16(4, 2, (1, 1, n, d))
+    o, lse = run_gpu(q, k, v, 1.0 / math.sqrt(d), causal)
+    cnt = np.arange(1, n + 1) if causal else np.full(n, n)
+    assert np.max(np.abs(lse[0, 0] - np.log(cnt))) < 1e-5
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v, 1.0 / math.sqrt(d), causal)
+    assert_close(o, lse, o_ref, lse_ref, "zero keys")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("sigma_q", [8.0, 30.0])
+def test_wide_logits_force_rescaling(d, sigma_q):
+    """Large, spread logits: the running maximum moves by far more than tau many times."""
+    w = synth.Workload("wide", 1, 2, 1100, 1100, d, True, sigma_q=sigma_q, seed=41)
+    _check_full(w)
+    _check_full(w.with_(causal=False, seed=42))
+
+
+def test_increasing_logits_rescale_every_tile():
+    """Keys sorted so that every new tile raises each row's maximum."""
+    n, d = 1024, 64
+    rng = np.random.default_rng(8)
+    q = np.zeros((1, 1, n, d), dtype=np.float32)
+    q[..., 0] = 1.0
+    k = np.zeros((1, 1, n, d), dtype=np.float32)
+    k[..., 0] = np.linspace(-40.0, 40.0, n)  # logits grow along the key axis
+    v = rng.normal(size=(1, 1, n, d)).astype(np.float32)
+    bits = [synth.f32_to_bf16_bits(x) for x in (q, k, v)]
+    for causal in (False, True):
+        o, lse = run_gpu(*bits, 1.0, causal)
+        o_ref, lse_ref = oracle.attention_fwd(*bits, 1.0, causal)
+        assert_close(o, lse, o_ref, lse_ref, f"increasing causal={causal}")
+
+
+def test_constant_values():
+    w = synth.Workload("const", 1, 2, 777, 777, 128, True, seed=5)
+    q, k, _ = w.make()
+    v = np.full(k.shape, synth.f32_to_bf16_bits(np.float32([1.5]))[0], dtype=np.uint16)
+    o, _ = run_gpu(q, k, v, w.scale, True)
+    assert np.max(np.abs(o - 1.5)) <= 1.5 * 2 ** -8
+
+
+def test_empty_query_rows_noop():
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    q = torch.zeros((1, 1, 0, 64), dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros((1, 1, 5, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = fa.fwd(q, k, k)
+    assert o.shape == (1, 1, 0, 64) and lse.shape == (1, 1, 0)
+
+
+def test_deterministic():
+    w = synth.Workload("det", 2, 3, 1000, 1000, 128, True, seed=9)
+    q, k, v = w.make()
+    o1, l1 = run_gpu(q, k, v, w.scale, True)
+    o2, l2 = run_gpu(q, k, v, w.scale, True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_outputs_not_written_outside(d=128):
+    """O and LSE buffers embedded in larger guard-filled buffers: guards untouched."""
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    w = synth.Workload("guard", 1, 2, 333, 333, d, True, seed=10)
+    q, k, v = w.make()
+    tq, tk, tv = to_device(q), to_device(k), to_device(v)
+    n_o = q.size
+    big_o = torch.full((n_o + 2 * 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    big_l = torch.full((2 * 333 + 2 * 64,), -3.0, dtype=torch.float32, device="cuda")
+    o = big_o[4096:4096 + n_o].view(q.shape)
+    lse = big_l[64:64 + 2 * 333].view(1, 2, 333)
+    fa.fwd(tq, tk, tv, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    assert torch.all(big_o[:4096] == 7.0) and torch.all(big_o[4096 + n_o:] == 7.0)
+    assert torch.all(big_l[:64] == -3.0) and torch.all(big_l[64 + 666:] == -3.0)
+
+
+# --- device-side argument errors -------------------------------------------------
+def test_host_pointer_rejected():
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    qh = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16)  # host memory
+    qd = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(qd)
+    lse = torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
+    st = fa.fa_fwd(qh.data_ptr(), qd.data_ptr(), qd.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 128, 128,
+                   64, 0.125, 0, None)
+    assert st == 10  # FA_ERR_POINTER
+
+
+# --- full benchmark sizes, sampled rows --------------------------------------------
+@pytest.mark.parametrize("name", ["long_8192_d128", "long_8192_d128_causal", "stress_32000_d128_causal"])
+def test_full_size_sampled_rows(name):
+    w = synth.WORKLOADS[name]
+    q, k, v = w.make()
+    o, lse = run_gpu(q, k, v, w.scale, w.causal)
+    rows = sample_rows(w.B, w.H, w.Nq, 400, seed=w.seed)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, rows, w.scale, w.causal)
+    o_s = o.reshape(-1, w.d)[rows]
+    l_s = lse.reshape(-1)[rows]
+    assert_close(o_s, l_s, o_ref, lse_ref, name)
+    # properties over every row at full size
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    if w.causal:
+        # row 0 of every head sees key 0 only: O = V[0] exactly, LSE = scale * q0.k0
+        vv = synth.bf16_to_f32(v[:, :, 0, :]).astype(np.float64)
+        assert np.array_equal(o[:, :, 0, :], vv)
