@@ -1,0 +1,437 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused exact-attention forward on GB300.
+
+One step = one fa_fwd call over the whole workload (all heads, all query
+tiles, every visible K/V tile).  Default workload: long context, B=4 H=32
+Nq=Nk=8192 d=128, non-causal, bf16 Q/K/V ~ N(0, 1) (synthetic, seeded).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  Metric: attention forward TFLOP/s with
+FLOPs = 4*B*H*Nq*Nk*d (halved when causal), plus the fraction of the measured
+dense-bf16 peak.  Under torchrun each rank runs the same workload on its own
+GPU (independent replicas, weak scaling); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak (1 GPU)"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "long_8192_d128"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_NAME = "fa_fwd_kernel"
+KERNEL_SOURCES = ["exact_attention_19_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_19_gb300/csrc/fa_ptx.cuh",
+                  "exact_attention_19_gb300/csrc/fa_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_kernel_dram_traffic.md")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+# ----------------------------------------------------------------------------
+# small helpers (host logic, testable without a GPU)
+# ----------------------------------------------------------------------------
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic(workload: str, src_hash: str):
+    """DRAM bytes per launch recorded by an ncu capture of this exact kernel source, else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    pat = re.compile(r"^\|\s*" + re.escape(workload) + r"\s*\|\s*([0-9a-f]{16})\s*\|\s*([0-9.eE+]+)\s*\|")
+    with open(TRAFFIC_FILE) as f:
+        for line in f:
+            m = pat.match(line.strip())
+            if m and m.group(1) == src_hash:
+                return float(m.group(2))
+    return None
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def visible_keys(w: synth.Workload, rows: np.ndarray) -> np.ndarray:
+    i = rows % w.Nq
+    return np.minimum(i + 1, w.Nk) if w.causal else np.full(rows.shape, w.Nk)
+
+
+def sample_rows_even(w: synth.Workload, n: int) -> np.ndarray:
+    total = w.B * w.H * w.Nq
+    n = max(1, min(n, total))
+    return np.unique(np.linspace(0, total - 1, n).round().astype(np.int64))
+
+
+def max_over_ranks(values, dist=None, device="cpu"):
+    """Element-wise max of a list of floats over all ranks (identity without a process group)."""
+    if dist is None:
+        return [float(x) for x in values]
+    import torch
+
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def aggregate(elapsed_ms_per_rank, flops_per_rank):
+    """Whole-job throughput: all ranks' FLOPs over the slowest rank's time."""
+    t = max(elapsed_ms_per_rank)
+    return sum(flops_per_rank) / (t * 1e-3) / 1e12, t
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background; keep (time, row)."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(self.FIELDS), "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for (t, s) in self.samples if t0 <= t <= t1]
+        if not inside and self.samples:  # region shorter than the sampling period: nearest sample
+            mid = 0.5 * (t0 + t1)
+            inside = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(s[0]) for s in inside if num(s[0]) is not None]
+        smax = [num(s[1]) for s in inside if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if s[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------
+# CPU oracle leg (the reference arm and the cpu_baseline field)
+# ----------------------------------------------------------------------------
+def time_oracle(w: synth.Workload, q, k, v, budget_s: float, max_rows: int | None = None):
+    """Run the oracle on an even sample of rows sized to about budget_s.
+
+    Returns (TFLOP/s, seconds, rows, threads)."""
+    import oracle
+
+    # calibrate: a warm-up call (thread pool, page faults), then grow the
+    # sample until one call takes a measurable fraction of the budget
+    n_probe = 16
+    oracle.attention_rows(q, k, v, sample_rows_even(w, n_probe), w.scale, w.causal)
+    while True:
+        probe = sample_rows_even(w, n_probe)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, probe, w.scale, w.causal)
+        t_probe = max(time.perf_counter() - t0, 1e-6)
+        if t_probe >= 0.05 * budget_s or probe.size >= w.B * w.H * w.Nq:
+            break
+        n_probe *= 4
+    n = int(len(probe) * budget_s / t_probe)
+    if max_rows:
+        n = min(n, max_rows)
+    rows = sample_rows_even(w, max(n, 16))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, rows, w.scale, w.causal)
+    secs = time.perf_counter() - t0
+    flops = float(np.sum(4.0 * visible_keys(w, rows) * w.d))
+    return flops / secs / 1e12, secs, int(rows.size), oracle.threads()
+
+
+def run_reference(args, w: synth.Workload, rank: int):
+    if rank != 0:
+        return 0
+    import oracle
+
+    oracle.build()
+    q, k, v = w.make()
+    steps, warmup = args.steps, args.warmup
+    per_step = max(0.05, min(2.0, 150.0 / max(1, steps + warmup)))
+    for _ in range(warmup):
+        time_oracle(w, q, k, v, per_step)
+    total_flops, total_s, total_rows, threads = 0.0, 0.0, 0, oracle.threads()
+    for _ in range(steps):
+        tflops, secs, n, threads = time_oracle(w, q, k, v, per_step)
+        total_flops += tflops * 1e12 * secs
+        total_s += secs
+        total_rows += n
+    value = total_flops / total_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": warmup, "ms_per_step": total_s / steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{total_rows // steps} evenly spaced query rows of {w.name} per step "
+                                   f"(of {w.B * w.H * w.Nq}); fp64 C oracle, OpenMP"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_of(w: synth.Workload, l2_note: str | None = None):
+    c = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
+         "scale": w.scale, "inputs": f"bf16 q~N(0,{w.sigma_q:g}^2), k,v~N(0,1), seed {w.seed}",
+         "flops_per_step": w.flops}
+    if l2_note:
+        c["l2"] = l2_note
+    return c
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
+    import torch
+
+    import exact_attention_19_gb300 as fa
+    from exact_attention_19_gb300 import build as fa_build
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa_build.build()
+    fa.load()
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    q_h, k_h, v_h = w.make()  # bf16 bits, host
+
+    def pinned(bits):
+        t = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    q_p, k_p, v_p = pinned(q_h), pinned(k_h), pinned(v_h)
+    q, k, v = q_p.to(dev), k_p.to(dev), v_p.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Nq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = 2 * (q.numel() + k.numel() + v.numel())
+    big_inputs = in_bytes > L2_BYTES
+    flush = None if big_inputs else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    l2_note = (f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB)" if big_inputs
+               else f"L2 flushed between timed steps ({2 * L2_BYTES / 1e6:.0f} MB write)")
+
+    def step():
+        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st, word = fa.fa_fwd_status(None, clear=True)
+    if st != 0:
+        raise RuntimeError(f"kernel reported a wait timeout during warm-up (status {word:#x})")
+
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local_rank)
+    except Exception:
+        gpu_id = str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+
+    # ---- device-timed steps ------------------------------------------------
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    if big_inputs:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        elapsed = e0.elapsed_time(e1)
+    else:
+        elapsed = 0.0
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            elapsed += e0.elapsed_time(e1)
+    barrier()
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
+    st, word = fa.fa_fwd_status(None, clear=True)
+    if st != 0:
+        raise RuntimeError(f"kernel reported a wait timeout (status {word:#x})")
+
+    # ---- end-to-end through the public API with host buffers ----------------
+    o_host = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        qd.copy_(q_p, non_blocking=True)
+        kd.copy_(k_p, non_blocking=True)
+        vd.copy_(v_p, non_blocking=True)
+        fa.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream)
+        o_host.copy_(o, non_blocking=True)
+        lse_host.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, 50))
+    e2e_ms = float("nan")
+    if not args.no_e2e:
+        for _ in range(min(args.warmup, 3)):
+            e2e_step()
+        barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        barrier()
+
+    # ---- max over ranks -------------------------------------------------------
+    t_max_elapsed, t_max_e2e = max_over_ranks([elapsed, e2e_ms], dist, dev)
+    times = [t_max_elapsed] * world
+    e2e_times = [t_max_e2e] * world
+    value, t_max = aggregate(times, [w.flops * args.steps] * world)
+    e2e_value, _ = aggregate(e2e_times, [w.flops] * world)
+    ms_per_step = t_max / args.steps
+
+    if rank != 0:
+        return 0
+
+    peaks, peaks_kind = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = w.flops / (ms_per_step * 1e-3) / 1e12
+    src_hash = kernel_source_hash()
+    traffic = read_traffic(w.name, src_hash)
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic, "peak_kind": f"bf16 burst, {peaks_kind}",
+                "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                "kernel": KERNEL_NAME, "kernel_source": src_hash,
+                "algorithmic_bytes": w.algorithmic_bytes,
+                "achieved_gbs": w.algorithmic_bytes / (ms_per_step * 1e-3) / 1e9}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        q_np, k_np, v_np = q_h, k_h, v_h
+        c_val, c_secs, c_rows, c_threads = time_oracle(w, q_np, k_np, v_np, args.cpu_seconds)
+        cpu = {"value": c_val, "unit": UNIT, "cores": c_threads, "kind": "oracle",
+               "sample": f"{c_rows} evenly spaced query rows of {w.B * w.H * w.Nq} ({c_secs:.1f} s, fp64 C "
+                         f"oracle, OpenMP)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w, l2_note),
+        "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(in_bytes),
+                "d2h_bytes_per_step": int(2 * o.numel() + 4 * lse.numel()), "ms_per_step": e2e_ms,
+                "steps": e2e_steps},
+        "gpu_launches": args.steps, "clocks": clocks,
+        "pct_of_peak": 100.0 * achieved / peak,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = synth.WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, w, rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    try:
+        return run_gpu(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,97 @@
+"""bench.py host logic without a GPU: throughput aggregation, max over ranks
+(two gloo ranks on CPU), traffic lookup and the oracle (reference) arm."""
+import contextlib
+import io
+import json
+import os
+import socket
+
+import numpy as np
+import pytest
+
+import bench
+import synth
+
+
+def test_aggregate_uses_slowest_rank():
+    v, t = bench.aggregate([2.0, 4.0], [1e12, 1e12])
+    assert t == 4.0 and v == pytest.approx(2e12 / 4e-3 / 1e12)
+
+
+def test_visible_keys_and_sampling():
+    w = synth.Workload("t", 1, 2, 10, 10, 64, True)
+    rows = np.arange(20)
+    assert bench.visible_keys(w, rows).tolist() == list(range(1, 11)) * 2
+    # over all rows the counted FLOPs equal the full-causal count up to the diagonal half
+    assert np.sum(4.0 * bench.visible_keys(w, rows) * 64) == pytest.approx(4 * 2 * 64 * (10 * 11 / 2))
+    r = bench.sample_rows_even(w, 7)
+    assert r[0] == 0 and r[-1] == 19 and len(set(r)) == len(r)
+
+
+def test_traffic_lookup(tmp_path, monkeypatch):
+    h = bench.kernel_source_hash()
+    f = tmp_path / "traffic.md"
+    f.write_text(f"| long_8192_d128 | {h} | 123456 | 1 | 2 | 3 | cmd |\n| other | {h} | 7 | | | | |\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.read_traffic("long_8192_d128", h) == 123456.0
+    assert bench.read_traffic("long_8192_d128", "0" * 16) is None
+    assert bench.read_traffic("missing", h) is None
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        elapsed = [10.0, 30.0][rank]
+        e2e = [7.0, 5.0][rank]
+        tmax, emax = bench.max_over_ranks([elapsed, e2e], dist, "cpu")
+        value, t = bench.aggregate([tmax] * world, [1e12 * 3] * world)
+        with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+            json.dump({"tmax": tmax, "emax": emax, "value": value}, f)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks(tmp_path):
+    import torch.multiprocessing as mp
+
+    port = _free_port()
+    mp.start_processes(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
+    res = [json.load(open(tmp_path / f"r{r}.json")) for r in range(2)]
+    for r in res:
+        assert r["tmax"] == 30.0 and r["emax"] == 7.0
+        assert r["value"] == pytest.approx(2 * 3e12 / 30e-3 / 1e12)
+
+
+def test_reference_arm_line(monkeypatch):
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--workload",
+                         "single_head_256_d64"])
+    assert rc == 0
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "single_head_256_d64"
+
+
+def test_reference_arm_other_ranks_silent(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
+    assert rc == 0 and buf.getvalue() == ""
