@@ -17,16 +17,16 @@
 // GB300 mapping (one CTA per SM, 320 threads):
 //   warps 0-3  softmax + correction + epilogue for query tile 0 (TMEM lanes 0-127)
 //   warps 4-7  the same for query tile 1
-//   warp  8    TMA producer: Q tiles once, K/V tiles through a ring of
-//              `kStages` stages each (mbarrier full/empty pairs)
+//   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through
+//              one ring of kRing tile-sized slots (mbarrier full/empty per slot)
 //   warp  9    MMA issuer: tcgen05.mma (one thread), commits to mbarriers
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D);
 //   P_i (bf16, packed in pairs) overwrites the first 64 columns of S_i and is
 //   the A operand of GEMM-II straight from TMEM.
-// Shared memory: Q0, Q1, K ring, V ring; each tile 128 rows x D bf16 stored
-// as D/64 boxes of 128 rows x 128 bytes with the 128-byte swizzle that TMA
-// writes and the MMA descriptors read (K-major for Q and K, MN-major for V).
+// Shared memory: Q0, Q1, then the K/V ring; each tile is 128 rows x D bf16
+// stored as D/64 boxes of 128 rows x 128 bytes with the 128-byte swizzle that
+// TMA writes and the MMA descriptors read (K-major for Q and K, MN-major for V).
 #pragma once
 
 #include <cstdint>
@@ -54,23 +54,26 @@ struct Cfg {
   static constexpr int kThreads = 320;
   static constexpr int kBM = 128;  // query rows per tile (MMA M)
   static constexpr int kBN = 128;  // keys per tile
-  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kRing = (D == 128) ? 5 : 8;  // K/V ring slots (K and V alternate)
   static constexpr int kBoxes = D / 64;  // 128-byte swizzle boxes per row
   static constexpr uint32_t kBoxBytes = 128u * 128u;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
   static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKOff = 2 * kTileBytes;
-  static constexpr uint32_t kVOff = kKOff + kStages * kTileBytes;
-  static constexpr uint32_t kBarOff = kVOff + kStages * kTileBytes;
-  static constexpr uint32_t kSmemBytes = kBarOff + 256 + 1024;  // barriers, then alignment slack
+  static constexpr uint32_t kRingOff = 2 * kTileBytes;
+  static constexpr uint32_t kBarOff = kRingOff + kRing * kTileBytes;
+  static constexpr uint32_t kBarBytes = 512;
+  static constexpr uint32_t kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
   static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);  // S = Q K^T
   static constexpr uint32_t kIdescO = idesc_bf16(128, D, true);     // O += P V
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-// barrier slots (8 bytes each) inside the barrier block
+// barrier slots (8 bytes each) inside the barrier block; the ring's full
+// barriers start at kBarRing, its empty barriers right after them
 enum : int { kBarQ = 0, kBarS = 2, kBarP = 4, kBarO = 6, kBarDrain = 8, kBarRing = 9 };
+constexpr uint32_t kTmemSlotOff = 448, kAbortOff = 452;
 
 __device__ __forceinline__ void report_wait_failure(volatile int* abort, unsigned role) {
   *abort = 1;
@@ -89,10 +92,11 @@ __global__ void __launch_bounds__(320, 1)
 
   const uint32_t bar0 = base + C::kBarOff;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const int kBarKFull = kBarRing, kBarKEmpty = kBarRing + C::kStages;
-  const int kBarVFull = kBarRing + 2 * C::kStages, kBarVEmpty = kBarRing + 3 * C::kStages;
-  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::kBarOff + 192);
-  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + C::kBarOff + 196);
+  auto full = [&](int slot) -> uint32_t { return bar(kBarRing + slot); };
+  auto empty = [&](int slot) -> uint32_t { return bar(kBarRing + C::kRing + slot); };
+  auto slot_addr = [&](int slot) -> uint32_t { return base + C::kRingOff + slot * C::kTileBytes; };
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::kBarOff + kTmemSlotOff);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + C::kBarOff + kAbortOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -107,11 +111,9 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(kBarO + 0), 1);
     mbar_init(bar(kBarO + 1), 1);
     mbar_init(bar(kBarDrain), 1);
-    for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(bar(kBarKFull + s), 1);
-      mbar_init(bar(kBarKEmpty + s), 1);
-      mbar_init(bar(kBarVFull + s), 1);
-      mbar_init(bar(kBarVEmpty + s), 1);
+    for (int s = 0; s < C::kRing; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -138,6 +140,7 @@ __global__ void __launch_bounds__(320, 1)
     nkv[t] = (row0[t] < p.Nq) ? (CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all) : 0;
   }
   const int n_max = max(nkv[0], nkv[1]);
+  const int n_items = 2 * n_max;  // ring items: K_j = item 2j, V_j = item 2j+1
 
   if (warp == 8) {
     // ======================= TMA producer =================================
@@ -152,43 +155,25 @@ __global__ void __launch_bounds__(320, 1)
         for (int b = 0; b < C::kBoxes; ++b)
           tma_load_3d(dst + b * C::kBoxBytes, &tmQ, bar(kBarQ + t), b * 64, row0[t], bh);
       }
-      int issued = 0;  // K/V tiles issued
-      bool failed = false;
-      for (int j = 0; j < n_max; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t ph = (j / C::kStages) & 1;
-        if (!mbar_wait(bar(kBarKEmpty + s), ph ^ 1u, abort_flag)) { failed = true; break; }
-        mbar_arrive_expect_tx(bar(kBarKFull + s), C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(base + C::kKOff + s * C::kTileBytes + b * C::kBoxBytes, &tmK, bar(kBarKFull + s),
-                      b * 64, j * C::kBN, bh);
-        if (!mbar_wait(bar(kBarVEmpty + s), ph ^ 1u, abort_flag)) {
-          failed = true;
-          issued = -(j + 1);  // K of tile j issued, V not
+      int issued = 0;
+      for (int item = 0; item < n_items; ++item) {
+        const int s = item % C::kRing;
+        const uint32_t ph = (item / C::kRing) & 1;
+        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
+          report_wait_failure(abort_flag, 2u);
           break;
         }
-        mbar_arrive_expect_tx(bar(kBarVFull + s), C::kTileBytes);
+        const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
+        mbar_arrive_expect_tx(full(s), C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(base + C::kVOff + s * C::kTileBytes + b * C::kBoxBytes, &tmV, bar(kBarVFull + s),
-                      b * 64, j * C::kBN, bh);
-        issued = j + 1;
-      }
-      if (failed) {
-        report_wait_failure(abort_flag, 2u);
+          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (item >> 1) * C::kBN, bh);
+        issued = item + 1;
       }
       if (*abort_flag) {
-        // Let every copy already issued land before the CTA can exit.
-        const int nk = issued >= 0 ? issued : -issued;
-        const int nv = issued >= 0 ? issued : -issued - 1;
-        for (int s = 0; s < C::kStages; ++s) {
-          int jk = -1, jv = -1;
-          for (int j = 0; j < nk; ++j)
-            if (j % C::kStages == s) jk = j;
-          for (int j = 0; j < nv; ++j)
-            if (j % C::kStages == s) jv = j;
-          if (jk >= 0) mbar_wait(bar(kBarKFull + s), (jk / C::kStages) & 1, nullptr);
-          if (jv >= 0) mbar_wait(bar(kBarVFull + s), (jv / C::kStages) & 1, nullptr);
-        }
+        // Let every copy already issued land before the CTA can exit: the
+        // last item issued into each slot is among the final kRing items.
+        for (int item = max(0, issued - C::kRing); item < issued; ++item)
+          mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, nullptr);
         for (int t = 0; t < 2; ++t)
           if (nkv[t] > 0) mbar_wait(bar(kBarQ + t), 0, nullptr);
       }
@@ -201,8 +186,7 @@ __global__ void __launch_bounds__(320, 1)
       const uint32_t tO[2] = {tmem + C::kTmO0, tmem + C::kTmO1};
       // GEMM-I: S_t = Q_t K^T over D/16 k-steps of 16 (K-major, 128B swizzle:
       // k-step kk lives in box kk/4 at byte offset 32*(kk%4) of each row).
-      auto gemm1 = [&](int t, int s) {
-        const uint32_t sK = base + C::kKOff + s * C::kTileBytes;
+      auto gemm1 = [&](int t, uint32_t sK) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
@@ -213,59 +197,61 @@ __global__ void __launch_bounds__(320, 1)
       // GEMM-II: O_t += P_t V over 128/16 k-steps; P_t from TMEM (8 columns of
       // packed bf16 pairs per step), V MN-major: 16 keys = 2048 bytes per step,
       // second 64-column box of V at LBO = one box.
-      auto gemm2 = [&](int t, int s, bool acc_prev) {
-        const uint32_t sV = base + C::kVOff + s * C::kTileBytes;
+      auto gemm2 = [&](int t, uint32_t sV, bool acc_prev) {
 #pragma unroll
         for (int kk = 0; kk < C::kBN / 16; ++kk) {
           mma_ts(tO[t], tS[t] + kk * 8, sdesc_sw128(sV + kk * 2048, C::kBoxBytes, 1024), C::kIdescO,
                  (acc_prev || kk > 0) ? 1u : 0u);
         }
       };
+      auto wait_item = [&](int item) -> bool {
+        return mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, abort_flag);
+      };
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
         if (nkv[t] > 0) ok = mbar_wait(bar(kBarQ + t), 0, abort_flag);
-      if (ok && n_max > 0) ok = mbar_wait(bar(kBarKFull + 0), 0, abort_flag);
+      if (ok && n_max > 0) ok = wait_item(0);
       if (ok && n_max > 0) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
           if (nkv[t] > 0) {
-            gemm1(t, 0);
+            gemm1(t, slot_addr(0));
             mma_commit(bar(kBarS + t));
           }
-        mma_commit(bar(kBarKEmpty + 0));
+        mma_commit(empty(0));
       }
+      // Issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
       for (int j = 0; ok && j < n_max; ++j) {
-        const int sv = j % C::kStages;
+        const int iv = 2 * j + 1, ik = 2 * j + 2;  // ring items of V_j and K_{j+1}
         const bool has_next = (j + 1) < n_max;
-        const int sk = (j + 1) % C::kStages;
-        if (!(ok = mbar_wait(bar(kBarVFull + sv), (j / C::kStages) & 1, abort_flag))) break;
+        if (!(ok = wait_item(iv))) break;
         tc_fence_after();
         if (j < nkv[0]) {
           if (!(ok = mbar_wait(bar(kBarP + 0), j & 1, abort_flag))) break;
           tc_fence_after();
-          gemm2(0, sv, j > 0);
+          gemm2(0, slot_addr(iv % C::kRing), j > 0);
           if (j == nkv[0] - 1) mma_commit(bar(kBarO + 0));
         }
         if (has_next) {
-          if (!(ok = mbar_wait(bar(kBarKFull + sk), ((j + 1) / C::kStages) & 1, abort_flag))) break;
+          if (!(ok = wait_item(ik))) break;
           tc_fence_after();
         }
         if (j + 1 < nkv[0]) {
-          gemm1(0, sk);
+          gemm1(0, slot_addr(ik % C::kRing));
           mma_commit(bar(kBarS + 0));
         }
         if (j < nkv[1]) {
           if (!(ok = mbar_wait(bar(kBarP + 1), j & 1, abort_flag))) break;
           tc_fence_after();
-          gemm2(1, sv, j > 0);
+          gemm2(1, slot_addr(iv % C::kRing), j > 0);
           if (j == nkv[1] - 1) mma_commit(bar(kBarO + 1));
         }
-        mma_commit(bar(kBarVEmpty + sv));
+        mma_commit(empty(iv % C::kRing));
         if (j + 1 < nkv[1]) {
-          gemm1(1, sk);
+          gemm1(1, slot_addr(ik % C::kRing));
           mma_commit(bar(kBarS + 1));
         }
-        if (has_next) mma_commit(bar(kBarKEmpty + sk));
+        if (has_next) mma_commit(empty(ik % C::kRing));
       }
       if (!ok) report_wait_failure(abort_flag, 4u);
       // Drain: every MMA issued so far has completed once this barrier flips.
@@ -292,15 +278,15 @@ __global__ void __launch_bounds__(320, 1)
       got = __all_sync(0xffffffffu, got);
       if (!got) { ok = false; break; }
       tc_fence_after();
+      // S row in two halves: the second half's TMEM load overlaps the first
+      // half's row max.
       uint32_t s0[32], s1[32], s2[32], s3[32];
       tmem_ld32(tS + 0, s0);
       tmem_ld32(tS + 32, s1);
-      tmem_ld32(tS + 64, s2);
-      tmem_ld32(tS + 96, s3);
       tmem_ld_wait(s0);
       reg_pin(s1);
-      reg_pin(s2);
-      reg_pin(s3);
+      tmem_ld32(tS + 64, s2);
+      tmem_ld32(tS + 96, s3);
       float* const f0 = reinterpret_cast<float*>(s0);
       float* const f1 = reinterpret_cast<float*>(s1);
       float* const f2 = reinterpret_cast<float*>(s2);
@@ -309,27 +295,43 @@ __global__ void __launch_bounds__(320, 1)
       // masking: ragged key tail and the causal diagonal tile
       const bool tail = (j == n_kv_all - 1) && (p.Nk % C::kBN != 0);
       const bool diag = CAUSAL && (j == nt - 1);
-      if (tail || diag) {
-        int lim = p.Nk;
-        if (CAUSAL) lim = min(lim, row + 1);
-        lim -= j * C::kBN;  // columns >= lim are masked
+      const bool masked = tail || diag;
+      int lim = p.Nk;
+      if (CAUSAL) lim = min(lim, row + 1);
+      lim -= j * C::kBN;  // columns >= lim are masked
+      if (masked) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           if (i >= lim) f0[i] = NEG_INF;
           if (32 + i >= lim) f1[i] = NEG_INF;
+        }
+      }
+      float mx0 = fmax3(f0[0], f0[1], f1[0]), mx1 = fmax3(f0[2], f0[3], f1[1]);
+#pragma unroll
+      for (int i = 2; i < 16; ++i) {
+        if (i & 1) mx1 = fmax3(mx1, f0[2 * i], f0[2 * i + 1]);
+        else mx0 = fmax3(mx0, f0[2 * i], f0[2 * i + 1]);
+      }
+#pragma unroll
+      for (int i = 2; i < 32; i += 2) mx0 = fmax3(mx0, f1[i], f1[i + 1]);
+      tmem_ld_wait(s2);
+      reg_pin(s3);
+      if (masked) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
           if (64 + i >= lim) f2[i] = NEG_INF;
           if (96 + i >= lim) f3[i] = NEG_INF;
         }
       }
-      float mx0 = f0[0], mx1 = f1[0], mx2 = f2[0], mx3 = f3[0];
+      float mx2 = fmax3(f2[0], f2[1], f3[0]), mx3 = fmax3(f2[2], f2[3], f3[1]);
 #pragma unroll
-      for (int i = 1; i < 32; ++i) {
-        mx0 = fmaxf(mx0, f0[i]);
-        mx1 = fmaxf(mx1, f1[i]);
-        mx2 = fmaxf(mx2, f2[i]);
-        mx3 = fmaxf(mx3, f3[i]);
+      for (int i = 2; i < 16; ++i) {
+        if (i & 1) mx3 = fmax3(mx3, f2[2 * i], f2[2 * i + 1]);
+        else mx2 = fmax3(mx2, f2[2 * i], f2[2 * i + 1]);
       }
-      const float m_new = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * c;
+#pragma unroll
+      for (int i = 2; i < 32; i += 2) mx2 = fmax3(mx2, f3[i], f3[i + 1]);
+      const float m_new = fmaxf(fmax3(mx0, mx1, mx2), mx3) * c;
       const bool need = m_new > m_bar + 8.0f;
       const bool any_need = __any_sync(0xffffffffu, need);
       float alpha = 1.0f;
@@ -338,18 +340,19 @@ __global__ void __launch_bounds__(320, 1)
         m_bar = m_new;
         l *= alpha;
       }
-      const float m_ref = (m_bar == NEG_INF) ? 0.f : m_bar;
+      const float neg_ref = (m_bar == NEG_INF) ? 0.f : -m_bar;
       // P = 2^(S*c - m_ref), rounded to bf16 pairs into the first 64 columns
       // of this tile's S region (16 columns = 32 probabilities per store).
-      float ls0 = 0.f, ls1 = 0.f;
+      float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
       auto emit = [&](const float* f, uint32_t col) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float e0 = ex2(fmaf(f[2 * i], c, -m_ref));
-          const float e1 = ex2(fmaf(f[2 * i + 1], c, -m_ref));
-          ls0 += e0;
-          ls1 += e1;
+          float x0, x1;
+          fma2(x0, x1, f[2 * i], f[2 * i + 1], c, neg_ref);
+          const float e0 = ex2(x0), e1 = ex2(x1);
+          if (i & 1) add2(ls2, ls3, e0, e1);
+          else add2(ls0, ls1, e0, e1);
           pk[i] = pack_bf16(e0, e1);
         }
         tmem_st16(tS + col, pk);
@@ -358,7 +361,7 @@ __global__ void __launch_bounds__(320, 1)
       emit(f1, 16);
       emit(f2, 32);
       emit(f3, 48);
-      l += ls0 + ls1;
+      l += (ls0 + ls1) + (ls2 + ls3);
       // correction: O *= alpha for the rows whose reference moved (the
       // previous P V of this tile has completed: S of this tile was issued
       // after it and its commit covers it).

@@ -225,6 +225,36 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (d0, d1) = (a0 * b + c, a1 * b + c) as one packed f32x2 FMA
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 x, y, z, w;\n\t"
+      "mov.b64 x, {%2, %3};\n\t"
+      "mov.b64 y, {%4, %4};\n\t"
+      "mov.b64 z, {%5, %5};\n\t"
+      "fma.rn.f32x2 w, x, y, z;\n\t"
+      "mov.b64 {%0, %1}, w;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1) as one packed f32x2 add
+__device__ __forceinline__ void add2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 x, y, w;\n\t"
+      "mov.b64 x, {%0, %1};\n\t"
+      "mov.b64 y, {%2, %3};\n\t"
+      "add.rn.f32x2 w, x, y;\n\t"
+      "mov.b64 {%0, %1}, w;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
 // Pack two floats to bf16x2 (round to nearest even); `lo` lands in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t d;
