@@ -181,28 +181,28 @@ __global__ void __launch_bounds__(320, 1)
   } else if (warp == 9) {
     // ======================= MMA issuer ====================================
     if (lane == 0) {
-      const uint32_t sQ[2] = {base + C::kQOff, base + C::kQOff + C::kTileBytes};
+      // descriptors: start address lives in bits 0-13 (address >> 4), so a
+      // byte offset is added to a base descriptor as (offset >> 4)
+      const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
+      const uint64_t dQ1 = sdesc_sw128(base + C::kQOff + C::kTileBytes, 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(base + C::kRingOff, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(base + C::kRingOff, C::kBoxBytes, 1024);
       const uint32_t tS[2] = {tmem + C::kTmS0, tmem + C::kTmS1};
       const uint32_t tO[2] = {tmem + C::kTmO0, tmem + C::kTmO1};
-      // GEMM-I: S_t = Q_t K^T over D/16 k-steps of 16 (K-major, 128B swizzle:
-      // k-step kk lives in box kk/4 at byte offset 32*(kk%4) of each row).
-      auto gemm1 = [&](int t, uint32_t sK) {
+      auto gemm1 = [&](int t, int slot) {
+        const uint64_t dq = t ? dQ1 : dQ0;
+        const uint64_t dk = dK0 + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kBoxBytes + (kk & 3) * 32;
-          mma_ss(tS[t], sdesc_sw128(sQ[t] + off, 16, 1024), sdesc_sw128(sK + off, 16, 1024), C::kIdescS,
-                 kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tS[t], dq + off, dk + off, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
-      // GEMM-II: O_t += P_t V over 128/16 k-steps; P_t from TMEM (8 columns of
-      // packed bf16 pairs per step), V MN-major: 16 keys = 2048 bytes per step,
-      // second 64-column box of V at LBO = one box.
-      auto gemm2 = [&](int t, uint32_t sV, bool acc_prev) {
+      auto gemm2 = [&](int t, int slot, bool acc_prev) {
+        const uint64_t dv = dV0 + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < C::kBN / 16; ++kk) {
-          mma_ts(tO[t], tS[t] + kk * 8, sdesc_sw128(sV + kk * 2048, C::kBoxBytes, 1024), C::kIdescO,
-                 (acc_prev || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < C::kBN / 16; ++kk)
+          mma_ts(tO[t], tS[t] + kk * 8, dv + ((kk * 2048) >> 4), C::kIdescO, (acc_prev || kk > 0) ? 1u : 0u);
       };
       auto wait_item = [&](int item) -> bool {
         return mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, abort_flag);
@@ -215,43 +215,42 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
           if (nkv[t] > 0) {
-            gemm1(t, slot_addr(0));
+            gemm1(t, 0);
             mma_commit(bar(kBarS + t));
           }
         mma_commit(empty(0));
       }
-      // Issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
+      // Issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), with
+      // every barrier check of the first half gathered in one place (each
+      // check behind queued MMAs costs a pipe bubble, consecutive ones cost one).
       for (int j = 0; ok && j < n_max; ++j) {
         const int iv = 2 * j + 1, ik = 2 * j + 2;  // ring items of V_j and K_{j+1}
+        const int sv = iv % C::kRing, sk = ik % C::kRing;
         const bool has_next = (j + 1) < n_max;
         if (!(ok = wait_item(iv))) break;
+        if (has_next && !(ok = wait_item(ik))) break;
+        if (j < nkv[0] && !(ok = mbar_wait(bar(kBarP + 0), j & 1, abort_flag))) break;
         tc_fence_after();
         if (j < nkv[0]) {
-          if (!(ok = mbar_wait(bar(kBarP + 0), j & 1, abort_flag))) break;
-          tc_fence_after();
-          gemm2(0, slot_addr(iv % C::kRing), j > 0);
+          gemm2(0, sv, j > 0);
           if (j == nkv[0] - 1) mma_commit(bar(kBarO + 0));
         }
-        if (has_next) {
-          if (!(ok = wait_item(ik))) break;
-          tc_fence_after();
-        }
         if (j + 1 < nkv[0]) {
-          gemm1(0, slot_addr(ik % C::kRing));
+          gemm1(0, sk);
           mma_commit(bar(kBarS + 0));
         }
         if (j < nkv[1]) {
           if (!(ok = mbar_wait(bar(kBarP + 1), j & 1, abort_flag))) break;
           tc_fence_after();
-          gemm2(1, slot_addr(iv % C::kRing), j > 0);
+          gemm2(1, sv, j > 0);
           if (j == nkv[1] - 1) mma_commit(bar(kBarO + 1));
         }
-        mma_commit(empty(iv % C::kRing));
+        mma_commit(empty(sv));
         if (j + 1 < nkv[1]) {
-          gemm1(1, slot_addr(ik % C::kRing));
+          gemm1(1, sk);
           mma_commit(bar(kBarS + 1));
         }
-        if (has_next) mma_commit(empty(ik % C::kRing));
+        if (has_next) mma_commit(empty(sk));
       }
       if (!ok) report_wait_failure(abort_flag, 4u);
       // Drain: every MMA issued so far has completed once this barrier flips.

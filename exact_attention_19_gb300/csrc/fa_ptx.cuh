@@ -201,6 +201,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : FA_R8(0), FA_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : FA_P8(0), FA_P8(8)::"memory");
+}
+
 // Wait for this thread's TMEM loads; the registers are threaded through the
 // asm so that no use of them can be scheduled before the wait.
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
