@@ -227,9 +227,17 @@ __global__ void __launch_bounds__(320, 1)
         const int iv = 2 * j + 1, ik = 2 * j + 2;  // ring items of V_j and K_{j+1}
         const int sv = iv % C::kRing, sk = ik % C::kRing;
         const bool has_next = (j + 1) < n_max;
-        if (!(ok = wait_item(iv))) break;
-        if (has_next && !(ok = wait_item(ik))) break;
-        if (j < nkv[0] && !(ok = mbar_wait(bar(kBarP + 0), j & 1, abort_flag))) break;
+        {
+          // the three checks are issued back to back so their latencies overlap
+          const bool a = mbar_try_wait(full(sv), (iv / C::kRing) & 1);
+          const bool b = !has_next || mbar_try_wait(full(sk), (ik / C::kRing) & 1);
+          const bool c = j >= nkv[0] || mbar_try_wait(bar(kBarP + 0), j & 1);
+          if (!(a && b && c)) {
+            if (!(ok = wait_item(iv))) break;
+            if (has_next && !(ok = wait_item(ik))) break;
+            if (j < nkv[0] && !(ok = mbar_wait(bar(kBarP + 0), j & 1, abort_flag))) break;
+          }
+        }
         tc_fence_after();
         if (j < nkv[0]) {
           gemm2(0, sv, j > 0);
