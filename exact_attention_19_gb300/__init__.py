@@ -15,8 +15,8 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "fa_fwd", "fa_strerror", "fa_version", "fa_fwd_status", "fwd", "library_path",
-           "load", "STATUS"]
+__all__ = ["FaError", "fa_fwd", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_splitkv_heuristic",
+           "fa_strerror", "fa_version", "fa_fwd_status", "fwd", "library_path", "load", "STATUS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libfa_gb300.so")
@@ -24,7 +24,7 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libfa_gb300.so")
 STATUS = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_ALIGN", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
     5: "FA_ERR_CAUSAL_SHAPE", 6: "FA_ERR_LAUNCH", 7: "FA_ERR_DEVICE", 8: "FA_ERR_TIMEOUT",
-    9: "FA_ERR_SCALE", 10: "FA_ERR_POINTER",
+    9: "FA_ERR_SCALE", 10: "FA_ERR_POINTER", 11: "FA_ERR_WORKSPACE",
 }
 
 _lib = None
@@ -57,6 +57,13 @@ def load():
         lib.fa_version.restype = i32
         lib.fa_fwd_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint), i32]
         lib.fa_fwd_status.restype = i32
+        lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp,
+                                       ctypes.c_size_t, vp]
+        lib.fa_fwd_splitkv.restype = i32
+        lib.fa_splitkv_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        lib.fa_splitkv_heuristic.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.fa_splitkv_heuristic.restype = i32
         _lib = lib
     return _lib
 
@@ -78,6 +85,21 @@ def fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream) -> int:
                              int(causal), stream))
 
 
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, workspace, workspace_bytes,
+                   stream) -> int:
+    """Raw C-ABI split-KV call; returns the status code (does not raise)."""
+    return int(load().fa_fwd_splitkv(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                                     int(causal), int(n_splits), workspace, int(workspace_bytes), stream))
+
+
+def fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits) -> int:
+    return int(load().fa_splitkv_workspace_bytes(int(B), int(H), int(Nq), int(Nk), int(d), int(n_splits)))
+
+
+def fa_splitkv_heuristic(B, H, Nq, Nk, d, causal) -> int:
+    return int(load().fa_splitkv_heuristic(int(B), int(H), int(Nq), int(Nk), int(d), int(causal)))
+
+
 def fa_fwd_status(stream=None, clear: bool = False):
     """(status, raw device status word) after synchronising ``stream``."""
     word = ctypes.c_uint(0)
@@ -93,13 +115,19 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None):
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
+        n_splits: int | None = None, workspace=None):
     """O = softmax(q k^T * scale) v and the per-row LSE, on the GPU.
 
     q: [B, H, Nq, d], k, v: [B, H, Nk, d] torch.bfloat16 CUDA tensors,
     contiguous.  ``scale`` defaults to 1/sqrt(d).  ``out`` (bf16 [B,H,Nq,d])
     and ``lse`` (fp32 [B,H,Nq]) may be given to avoid allocation.  Runs on
     ``stream`` (default: the current torch stream), asynchronously.
+
+    ``n_splits``: K/V slices per query tile (split-KV, for shapes with too few
+    query tiles to fill the GPU); None asks the library's heuristic, 1 forces
+    the single-pass kernel.  ``workspace`` (a CUDA tensor of at least
+    ``fa_splitkv_workspace_bytes`` bytes) may be given to avoid allocating it.
     """
     import torch
 
@@ -122,6 +150,20 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         raise ValueError("out must be a contiguous bf16 tensor shaped like q")
     if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    if n_splits is None:
+        n_splits = fa_splitkv_heuristic(B, H, Nq, Nk, d, int(bool(causal))) if Nq > 0 else 1
+    if n_splits > 1:
+        need = fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        if not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+            raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+        st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq,
+                            Nk, d, scale, int(bool(causal)), n_splits, workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+        if st != 0:
+            raise FaError(st, "fa_fwd_splitkv")
+        return out, lse
     st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk, d,
                 scale, int(bool(causal)), _stream_handle(stream))
     if st != 0:

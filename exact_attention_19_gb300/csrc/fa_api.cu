@@ -39,11 +39,16 @@ EncodeTiledFn encode_fn() {
 // Per-device one-time state: compute capability check and the kernels'
 // shared-memory opt-in.  0 = not yet, 1 = ready, -1 = unsupported device.
 std::atomic<int> g_dev_state[kMaxDevices];
+int g_dev_sms[kMaxDevices];  // multiprocessor count, valid once the state is 1
+
+int g_dev_sms_or(int dev, int fallback) {
+  return (dev >= 0 && dev < kMaxDevices && g_dev_sms[dev] > 0) ? g_dev_sms[dev] : fallback;
+}
 std::mutex g_dev_mutex;
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::Cfg<D>::kSmemBytes));
 }
 
@@ -63,8 +68,14 @@ int prepare_device(int dev) {
     g_dev_state[dev].store(-1, std::memory_order_release);
     return FA_ERR_DEVICE;
   }
-  if (set_smem_attr<64, false>() != cudaSuccess || set_smem_attr<64, true>() != cudaSuccess ||
-      set_smem_attr<128, false>() != cudaSuccess || set_smem_attr<128, true>() != cudaSuccess)
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return FA_ERR_LAUNCH;
+  g_dev_sms[dev] = sms;
+  if (set_smem_attr<64, false, false>() != cudaSuccess || set_smem_attr<64, true, false>() != cudaSuccess ||
+      set_smem_attr<128, false, false>() != cudaSuccess || set_smem_attr<128, true, false>() != cudaSuccess ||
+      set_smem_attr<64, false, true>() != cudaSuccess || set_smem_attr<64, true, true>() != cudaSuccess ||
+      set_smem_attr<128, false, true>() != cudaSuccess || set_smem_attr<128, true, true>() != cudaSuccess)
     return FA_ERR_LAUNCH;
   g_dev_state[dev].store(1, std::memory_order_release);
   return FA_OK;
@@ -95,12 +106,77 @@ bool make_map(CUtensorMap* map, const void* ptr, int D, long long N, long long B
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool SPLIT>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
            long long grid, cudaStream_t stream) {
-  fa::fa_fwd_kernel<D, CAUSAL><<<static_cast<unsigned>(grid), fa::Cfg<D>::kThreads, fa::Cfg<D>::kSmemBytes,
-                                 stream>>>(mq, mk, mv, p);
+  fa::fa_fwd_kernel<D, CAUSAL, SPLIT><<<static_cast<unsigned>(grid), fa::Cfg<D>::kThreads,
+                                        fa::Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+template <int D, bool SPLIT>
+int launch_d(bool causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+             const fa::FwdParams& p, long long grid, cudaStream_t stream) {
+  return causal ? launch<D, true, SPLIT>(mq, mk, mv, p, grid, stream)
+                : launch<D, false, SPLIT>(mq, mk, mv, p, grid, stream);
+}
+
+// Checks shared by fa_fwd and fa_fwd_splitkv.  On success fills the tensor
+// maps and the common parameters; *noop is set when Nq == 0.
+int prepare_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                 int d, float scale, int causal, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
+                 fa::FwdParams* p, int* dev_out, bool* noop) {
+  *noop = false;
+  // With Nq == 0 nothing is read or written, so the (empty) tensors may be NULL.
+  if ((Nq != 0 && (!q || !o || !lse)) || !k || !v) return FA_ERR_NULL;
+  const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
+                         reinterpret_cast<uintptr_t>(lse)) & 15u;
+  if (mis) return FA_ERR_ALIGN;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (B <= 0 || H <= 0 || Nk <= 0 || Nq < 0) return FA_ERR_SHAPE;
+  if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
+  if (causal && Nq != Nk) return FA_ERR_CAUSAL_SHAPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long n_pairs = (static_cast<long long>(Nq) + 255) / 256;
+  // tensor-map limits: a stride below 2^40 bytes, grid below 2^31 CTAs
+  if (static_cast<long long>(Nq > Nk ? Nq : Nk) * d * 2 >= (1ll << 40)) return FA_ERR_SHAPE;
+  if (BH >= (1ll << 31) || BH * n_pairs >= (1ll << 31)) return FA_ERR_SHAPE;
+  if (Nq == 0) {
+    *noop = true;
+    return FA_OK;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
+  const int prep = prepare_device(dev);
+  if (prep != FA_OK) return prep;
+  if (!is_device_pointer(q, dev) || !is_device_pointer(k, dev) || !is_device_pointer(v, dev) ||
+      !is_device_pointer(o, dev) || !is_device_pointer(lse, dev))
+    return FA_ERR_POINTER;
+  if (!make_map(mq, q, d, Nq, BH) || !make_map(mk, k, d, Nk, BH) || !make_map(mv, v, d, Nk, BH))
+    return FA_ERR_LAUNCH;
+  p->o = o;
+  p->lse = lse;
+  p->Nq = Nq;
+  p->Nk = Nk;
+  p->n_pairs = static_cast<int>(n_pairs);
+  p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  p->n_splits = 1;
+  p->split_tiles = 0;
+  p->o_part = nullptr;
+  p->lse_part = nullptr;
+  p->rows = BH * Nq;
+  *dev_out = dev;
+  return FA_OK;
+}
+
+// K/V tiles per split and the number of non-empty splits for a request.
+void split_shape(int Nk, int n_splits, int* split_tiles, int* eff_splits) {
+  const int n_kv = (Nk + 127) / 128;
+  const int req = n_splits < 1 ? 1 : (n_splits > n_kv ? n_kv : n_splits);
+  *split_tiles = (n_kv + req - 1) / req;
+  *eff_splits = (n_kv + *split_tiles - 1) / *split_tiles;
 }
 
 }  // namespace
@@ -122,55 +198,84 @@ const char* fa_strerror(int status) {
     case FA_ERR_TIMEOUT: return "a kernel wait timed out";
     case FA_ERR_SCALE: return "scale must be finite and > 0";
     case FA_ERR_POINTER: return "a tensor pointer is not device memory of the current device";
+    case FA_ERR_WORKSPACE: return "split-KV workspace is missing or smaller than fa_splitkv_workspace_bytes()";
     default: return "unknown status";
   }
 }
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
            int d, float scale, int causal, cudaStream_t stream) {
-  // ---- host-side validation (nothing is launched on failure) --------------
-  // With Nq == 0 nothing is read or written, so the (empty) tensors may be NULL.
-  if ((Nq != 0 && (!q || !o || !lse)) || !k || !v) return FA_ERR_NULL;
-  const uintptr_t mis = (reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                         reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o) |
-                         reinterpret_cast<uintptr_t>(lse)) & 15u;
-  if (mis) return FA_ERR_ALIGN;
-  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
-  if (B <= 0 || H <= 0 || Nk <= 0 || Nq < 0) return FA_ERR_SHAPE;
-  if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
-  if (causal && Nq != Nk) return FA_ERR_CAUSAL_SHAPE;
-  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
-  const long long BH = static_cast<long long>(B) * H;
-  const long long n_pairs = (static_cast<long long>(Nq) + 255) / 256;
-  const long long grid = BH * n_pairs;
-  // tensor-map limits: a stride below 2^40 bytes, grid below 2^31 CTAs
-  if (static_cast<long long>(Nq > Nk ? Nq : Nk) * d * 2 >= (1ll << 40)) return FA_ERR_SHAPE;
-  if (BH >= (1ll << 31) || grid >= (1ll << 31)) return FA_ERR_SHAPE;
-  if (Nq == 0) return FA_OK;
-
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
-  const int prep = prepare_device(dev);
-  if (prep != FA_OK) return prep;
-  if (!is_device_pointer(q, dev) || !is_device_pointer(k, dev) || !is_device_pointer(v, dev) ||
-      !is_device_pointer(o, dev) || !is_device_pointer(lse, dev))
-    return FA_ERR_POINTER;
-
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, d, Nq, BH) || !make_map(&mk, k, d, Nk, BH) || !make_map(&mv, v, d, Nk, BH))
-    return FA_ERR_LAUNCH;
-
   fa::FwdParams p;
-  p.o = o;
-  p.lse = lse;
-  p.Nq = Nq;
-  p.Nk = Nk;
-  p.n_pairs = static_cast<int>(n_pairs);
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  int dev = -1;
+  bool noop = false;
+  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &p, &dev, &noop);
+  if (st != FA_OK || noop) return st;
+  const long long grid = static_cast<long long>(B) * H * p.n_pairs;
+  return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, p, grid, stream)
+                 : launch_d<128, false>(causal, mq, mk, mv, p, grid, stream);
+}
 
-  if (d == 64) return causal ? launch<64, true>(mq, mk, mv, p, grid, stream)
-                             : launch<64, false>(mq, mk, mv, p, grid, stream);
-  return causal ? launch<128, true>(mq, mk, mv, p, grid, stream) : launch<128, false>(mq, mk, mv, p, grid, stream);
+size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_splits) {
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0 || (d != 64 && d != 128)) return 0;
+  int tiles = 0, eff = 0;
+  split_shape(Nk, n_splits, &tiles, &eff);
+  const size_t rows = static_cast<size_t>(B) * H * Nq;
+  return static_cast<size_t>(eff) * rows * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+int fa_splitkv_heuristic(int B, int H, int Nq, int Nk, int d, int causal) {
+  (void)d;
+  (void)causal;
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return 1;
+  int dev = -1, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess && prepare_device(dev) == FA_OK) sms = g_dev_sms_or(dev, sms);
+  const long long ctas = static_cast<long long>(B) * H * ((static_cast<long long>(Nq) + 255) / 256);
+  if (ctas >= sms) return 1;
+  const int n_kv = (Nk + 127) / 128;
+  long long want = sms / ctas;  // fill the SMs once
+  if (want > 16) want = 16;
+  if (want > n_kv / 2) want = n_kv / 2;  // a slice of one tile costs more than it saves
+  int tiles = 0, eff = 0;
+  split_shape(Nk, static_cast<int>(want < 1 ? 1 : want), &tiles, &eff);
+  return eff;
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                   int d, float scale, int causal, int n_splits, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
+  if (n_splits < 1 || n_splits > 64) return FA_ERR_SHAPE;
+  CUtensorMap mq, mk, mv;
+  fa::FwdParams p;
+  int dev = -1;
+  bool noop = false;
+  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &p, &dev, &noop);
+  if (st != FA_OK || noop) return st;
+  int tiles = 0, eff = 0;
+  split_shape(Nk, n_splits, &tiles, &eff);
+  if (eff == 1)  // one slice: the plain kernel, no workspace needed
+    return fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream);
+  const size_t need = fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits);
+  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
+  if (!is_device_pointer(workspace, dev)) return FA_ERR_POINTER;
+  p.n_splits = eff;
+  p.split_tiles = tiles;
+  p.o_part = static_cast<float*>(workspace);
+  p.lse_part = p.o_part + static_cast<size_t>(eff) * p.rows * d;
+  const long long grid = static_cast<long long>(B) * H * p.n_pairs * eff;
+  if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
+  const int rc = d == 64 ? launch_d<64, true>(causal, mq, mk, mv, p, grid, stream)
+                         : launch_d<128, true>(causal, mq, mk, mv, p, grid, stream);
+  if (rc != FA_OK) return rc;
+  const long long cgrid = (p.rows + 7) / 8;
+  if (d == 64)
+    fa::fa_splitkv_combine_kernel<64><<<static_cast<unsigned>(cgrid), 256, 0, stream>>>(p.o_part, p.lse_part, o, lse,
+                                                                                         p.rows, eff);
+  else
+    fa::fa_splitkv_combine_kernel<128><<<static_cast<unsigned>(cgrid), 256, 0, stream>>>(p.o_part, p.lse_part, o,
+                                                                                          lse, p.rows, eff);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear) {

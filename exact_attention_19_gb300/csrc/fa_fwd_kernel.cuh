@@ -44,8 +44,13 @@ struct FwdParams {
   void* o;            // bf16 [BH, Nq, D]
   float* lse;         // fp32 [BH, Nq]
   int Nq, Nk;
-  int n_pairs;        // ceil(Nq / 256): CTAs per (b, h)
+  int n_pairs;        // ceil(Nq / 256): query-tile pairs per (b, h)
   float scale_log2;   // scale * log2(e)
+  // split-KV only: CTAs per pair, K/V tiles per split, and the partial results
+  int n_splits, split_tiles;
+  float* o_part;      // fp32 [n_splits, BH * Nq, D], each slice normalised by its own l
+  float* lse_part;    // fp32 [n_splits, BH * Nq], m_bar + log2(l) in base-2 scaled units
+  long long rows;     // BH * Nq
 };
 
 template <int D>
@@ -80,7 +85,9 @@ __device__ __forceinline__ void report_wait_failure(volatile int* abort, unsigne
   atomicOr(&g_fa_status, 1u | (role << 8));
 }
 
-template <int D, bool CAUSAL>
+// SPLIT: the CTA covers K/V tiles [split * split_tiles, (split+1) * split_tiles)
+// of its pair and writes a partial result; fa_splitkv_combine_kernel merges them.
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -127,17 +134,25 @@ __global__ void __launch_bounds__(320, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // ---- work item: (b*H + h, pair of query tiles) --------------------------
-  const int bh = blockIdx.x / p.n_pairs;
-  int pair = blockIdx.x % p.n_pairs;
+  // ---- work item: (b*H + h, pair of query tiles[, K/V split]) -------------
+  int cta = blockIdx.x;
+  int split = 0;
+  if (SPLIT) {
+    split = cta % p.n_splits;
+    cta /= p.n_splits;
+  }
+  const int bh = cta / p.n_pairs;
+  int pair = cta % p.n_pairs;
   if (CAUSAL) pair = p.n_pairs - 1 - pair;  // heaviest pair of each head first
   const int n_kv_all = (p.Nk + C::kBN - 1) / C::kBN;
-  int row0[2], nkv[2];
+  const int kv_lo = SPLIT ? split * p.split_tiles : 0;  // first K/V tile of this CTA
+  int row0[2], nkv[2], nkv_full[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int qt = 2 * pair + t;
     row0[t] = qt * C::kBM;
-    nkv[t] = (row0[t] < p.Nq) ? (CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all) : 0;
+    nkv_full[t] = (row0[t] < p.Nq) ? (CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all) : 0;
+    nkv[t] = SPLIT ? max(0, min(nkv_full[t], kv_lo + p.split_tiles) - kv_lo) : nkv_full[t];
   }
   const int n_max = max(nkv[0], nkv[1]);
   const int n_items = 2 * n_max;  // ring items: K_j = item 2j, V_j = item 2j+1
@@ -166,7 +181,8 @@ __global__ void __launch_bounds__(320, 1)
         const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
         mbar_arrive_expect_tx(full(s), C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (item >> 1) * C::kBN, bh);
+          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (kv_lo + (item >> 1)) * C::kBN,
+                      bh);
         issued = item + 1;
       }
       if (*abort_flag) {
@@ -300,12 +316,13 @@ __global__ void __launch_bounds__(320, 1)
       float* const f3 = reinterpret_cast<float*>(s3);
 
       // masking: ragged key tail and the causal diagonal tile
-      const bool tail = (j == n_kv_all - 1) && (p.Nk % C::kBN != 0);
-      const bool diag = CAUSAL && (j == nt - 1);
+      const int jg = kv_lo + j;  // K/V tile index within the head
+      const bool tail = (jg == n_kv_all - 1) && (p.Nk % C::kBN != 0);
+      const bool diag = CAUSAL && (jg == nkv_full[t] - 1);
       const bool masked = tail || diag;
       int lim = p.Nk;
       if (CAUSAL) lim = min(lim, row + 1);
-      lim -= j * C::kBN;  // columns >= lim are masked
+      lim -= jg * C::kBN;  // columns >= lim are masked
       if (masked) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -397,28 +414,55 @@ __global__ void __launch_bounds__(320, 1)
         tc_fence_after();
         const float inv_l = (l > 0.f) ? (1.0f / l) : 0.f;
         const bool store = row < p.Nq;
-        uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                                     (static_cast<size_t>(bh) * p.Nq + row) * D);
+        const size_t grow = static_cast<size_t>(bh) * p.Nq + row;  // row within [BH * Nq]
+        if (!SPLIT) {
+          uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tO + cc * 32, o);
-          tmem_ld_wait(o);
-          uint32_t w[16];
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+            tmem_ld_wait(o);
+            uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (store) {
+            for (int i = 0; i < 16; ++i)
+              w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (store) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              orow[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                orow[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            }
           }
-        }
-        if (store) {
-          const float lse = (l > 0.f) ? (m_bar + __log2f(l)) * 0.69314718055994530942f : NEG_INF;
-          p.lse[static_cast<size_t>(bh) * p.Nq + row] = lse;
+          if (store) {
+            const float lse = (l > 0.f) ? (m_bar + __log2f(l)) * 0.69314718055994530942f : NEG_INF;
+            p.lse[grow] = lse;
+          }
+        } else {
+          // partial: O / l in fp32 and the base-2 log-sum-exp of this slice
+          const size_t prow = static_cast<size_t>(split) * p.rows + grow;
+          float4* const orow = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+            tmem_ld_wait(o);
+            if (store) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                orow[cc * 8 + i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                               __uint_as_float(o[4 * i + 2]) * inv_l,
+                                               __uint_as_float(o[4 * i + 3]) * inv_l);
+            }
+          }
+          if (store) p.lse_part[prow] = (l > 0.f) ? (m_bar + __log2f(l)) : NEG_INF;
         }
       }
+    } else if (SPLIT && ok && nt == 0 && row < p.Nq) {
+      // no visible key in this slice: an empty partial (weight 2^-inf = 0)
+      const size_t prow = static_cast<size_t>(split) * p.rows + static_cast<size_t>(bh) * p.Nq + row;
+      float4* const orow = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+      for (int i = 0; i < D / 4; ++i) orow[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      p.lse_part[prow] = NEG_INF;
     }
   }
 
@@ -430,6 +474,54 @@ __global__ void __launch_bounds__(320, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+}
+
+// Merge of split-KV partial results, one warp per query row: with slice
+// results (O_s, L_s) where O_s is normalised and L_s = log2 of its sum of
+// 2^(scaled logit), the row's O = sum_s 2^(L_s - L) O_s and L = log2 sum_s 2^L_s.
+// This is the order-insensitive merge of (m, l, O) states of the online
+// softmax (page "llm-infra-atlas / FlashAttention 01", section 2).
+template <int D>
+__global__ void __launch_bounds__(256) fa_splitkv_combine_kernel(const float* __restrict__ o_part,
+                                                                 const float* __restrict__ lse_part, void* o,
+                                                                 float* lse, long long rows, int n_splits) {
+  constexpr int kPer = D / 32;  // elements per lane
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float NEG_INF = -__int_as_float(0x7f800000);
+  float mx = NEG_INF;
+  for (int s = 0; s < n_splits; ++s) mx = fmaxf(mx, lse_part[static_cast<size_t>(s) * rows + row]);
+  float acc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  if (mx != NEG_INF) {
+    for (int s = 0; s < n_splits; ++s) {
+      const size_t prow = static_cast<size_t>(s) * rows + row;
+      const float w = ex2(lse_part[prow] - mx);
+      wsum += w;
+      const float* src = o_part + prow * D + lane * kPer;
+      if constexpr (kPer == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+        acc[2] += w * v.z;
+        acc[3] += w * v.w;
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * v.x;
+        acc[1] += w * v.y;
+      }
+    }
+  }
+  const float inv = wsum > 0.f ? 1.0f / wsum : 0.f;
+  uint16_t* orow = static_cast<uint16_t*>(o) + static_cast<size_t>(row) * D + lane * kPer;
+  if constexpr (kPer == 4)
+    *reinterpret_cast<uint2*>(orow) = make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
+  else
+    *reinterpret_cast<uint32_t*>(orow) = pack_bf16(acc[0] * inv, acc[1] * inv);
+  if (lane == 0) lse[row] = (wsum > 0.f) ? (mx + __log2f(wsum)) * 0.69314718055994530942f : NEG_INF;
 }
 
 }  // namespace fa

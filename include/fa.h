@@ -20,6 +20,8 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
+
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -38,7 +40,8 @@ typedef enum {
   FA_ERR_DEVICE = 7,        /* the current device is not compute capability 10.3 (GB300)  */
   FA_ERR_TIMEOUT = 8,       /* a kernel wait gave up (reported by fa_fwd_status)           */
   FA_ERR_SCALE = 9,         /* scale is not a finite positive number                       */
-  FA_ERR_POINTER = 10       /* a tensor pointer is not device memory of the current device */
+  FA_ERR_POINTER = 10,      /* a tensor pointer is not device memory of the current device */
+  FA_ERR_WORKSPACE = 11     /* split-KV workspace missing or smaller than required         */
 } fa_status;
 
 /*
@@ -71,6 +74,42 @@ typedef enum {
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
            int Nk, int d, float scale, int causal, cudaStream_t stream);
+
+/*
+ * fa_fwd_splitkv -- the same operation as fa_fwd, with each query tile's K/V
+ * range cut into n_splits slices processed by separate CTAs, for shapes whose
+ * B * H * ceil(Nq / 256) CTAs would leave most of the GPU idle.
+ *
+ * Each slice s produces a partial result for its rows: O_s normalised by its
+ * own row sum, and L_s = log2 of that row sum in base-2 scaled-logit units.
+ * A second kernel on the same stream merges the slices by the rule under which
+ * the online-softmax state (m, l, O) is insensitive to block order ("llm-infra-
+ * atlas / FlashAttention 01", section 2):
+ *   L = log2 sum_s 2^L_s,   O = sum_s 2^(L_s - L) O_s,   LSE = L * ln 2.
+ *
+ * Arguments as in fa_fwd, plus:
+ * n_splits   requested slices, 1..64; the call uses ceil(n_kv / ceil(n_kv /
+ *            n_splits)) of them, n_kv = ceil(Nk / 128).  With one slice this is
+ *            exactly fa_fwd and the workspace is not touched.
+ * workspace  device memory of at least fa_splitkv_workspace_bytes() bytes,
+ *            16-byte aligned, owned by the caller, not read before it is
+ *            written; it must not be used by anything else until the call's
+ *            kernels have finished on `stream`.
+ * Errors as fa_fwd, plus FA_ERR_SHAPE for n_splits outside 1..64 and
+ * FA_ERR_WORKSPACE for a missing or short workspace.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                   int Nk, int d, float scale, int causal, int n_splits, void* workspace,
+                   size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes fa_fwd_splitkv needs for these sizes (0 for invalid sizes):
+ * fp32 partial O [splits, B*H*Nq, d] followed by fp32 partial L [splits, B*H*Nq]. */
+size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_splits);
+
+/* Suggested n_splits for the current device: 1 when B * H * ceil(Nq / 256)
+ * CTAs already cover its multiprocessors, otherwise enough slices (at most 16,
+ * each of at least two K/V tiles) to fill them about once. */
+int fa_splitkv_heuristic(int B, int H, int Nq, int Nk, int d, int causal);
 
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* fa_strerror(int status);

@@ -21,14 +21,18 @@ def to_device(bits, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
 
-def run_gpu(q, k, v, scale, causal):
-    """q, k, v: uint16 bf16 bits [B,H,N,d].  Returns (o float64 numpy, lse float64 numpy)."""
+def run_gpu(q, k, v, scale, causal, n_splits=None):
+    """q, k, v: uint16 bf16 bits [B,H,N,d].  Returns (o float64 numpy, lse float64 numpy).
+
+    n_splits: None lets the library choose (split-KV for small grids), 1 forces
+    the single-pass kernel, > 1 forces that many K/V slices.
+    """
     import torch
 
     import exact_attention_19_gb300 as fa
 
     tq, tk, tv = to_device(q), to_device(k), to_device(v)
-    o, lse = fa.fwd(tq, tk, tv, causal=causal, scale=scale)
+    o, lse = fa.fwd(tq, tk, tv, causal=causal, scale=scale, n_splits=n_splits)
     torch.cuda.synchronize()
     st, word = fa.fa_fwd_status(None, clear=True)
     assert st == 0, f"kernel wait timed out, status word {word:#x}"

@@ -23,12 +23,13 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:int|const char\*|void)\s+(fa_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|const char\*|void|size_t)\s+(fa_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_entry_points():
     names = declared_functions()
-    assert {"fa_fwd", "fa_strerror", "fa_version", "fa_fwd_status"} <= set(names)
+    assert {"fa_fwd", "fa_strerror", "fa_version", "fa_fwd_status", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes",
+            "fa_splitkv_heuristic"} <= set(names)
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -43,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_version_and_strerror(lib):
     assert fa.fa_version() == 100
     assert fa.fa_strerror(0) == "ok"
-    for code in range(1, 11):
+    for code in range(1, 12):
         assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown status"
     assert fa.fa_strerror(12345) == "unknown status"
 
@@ -76,3 +77,27 @@ def test_empty_query_is_a_noop(lib):
     assert call(Nq=0) == 0
     assert call(Nq=0, q=None, o=None, lse=None) == 0
     assert call(Nq=0, k=None) == 1
+
+
+def test_splitkv_workspace_size(lib):
+    # n_kv = ceil(4096 / 128) = 32 tiles; 8 splits of 4 tiles; fp32 O [8, rows, 64] + L [8, rows]
+    assert fa.fa_splitkv_workspace_bytes(1, 1, 4096, 4096, 64, 8) == 8 * 4096 * 65 * 4
+    # 5 requested over 32 tiles -> 7 tiles per split -> 5 splits
+    assert fa.fa_splitkv_workspace_bytes(2, 3, 100, 4096, 128, 5) == 5 * 600 * 129 * 4
+    # more splits than tiles are capped at one split per tile
+    assert fa.fa_splitkv_workspace_bytes(1, 1, 10, 200, 64, 16) == 2 * 10 * 65 * 4
+    assert fa.fa_splitkv_workspace_bytes(1, 1, 10, 200, 96, 2) == 0
+    assert fa.fa_splitkv_workspace_bytes(0, 1, 10, 200, 64, 2) == 0
+
+
+@pytest.mark.parametrize("n_splits", [0, -1, 65])
+def test_splitkv_rejects_split_count(lib, n_splits):
+    st = fa.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 64, 0.125, 0, n_splits, FAKE, 1 << 20, None)
+    assert st == 3
+
+
+def test_splitkv_host_validation(lib):
+    st = fa.fa_fwd_splitkv(None, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 64, 0.125, 0, 2, FAKE, 1 << 20, None)
+    assert st == 1
+    st = fa.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 96, 0.125, 0, 2, FAKE, 1 << 20, None)
+    assert st == 4

@@ -30,34 +30,85 @@ def _gpu():
     yield
 
 
-def _check_full(w: synth.Workload):
+_ORACLE_CACHE = {}
+
+
+def _oracle_full(w: synth.Workload, q, k, v):
+    key = (w.B, w.H, w.Nq, w.Nk, w.d, w.causal, w.sigma_q, w.seed)
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = oracle.attention_fwd(q, k, v, w.scale, w.causal)
+    return _ORACLE_CACHE[key]
+
+
+def _check_full(w: synth.Workload, n_splits=None):
     q, k, v = w.make()
-    o, lse = run_gpu(q, k, v, w.scale, w.causal)
-    o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.scale, w.causal)
-    return assert_close(o, lse, o_ref, lse_ref, w.name)
+    o, lse = run_gpu(q, k, v, w.scale, w.causal, n_splits)
+    o_ref, lse_ref = _oracle_full(w, q, k, v)
+    return assert_close(o, lse, o_ref, lse_ref, f"{w.name} n_splits={n_splits}")
 
 
 # --- the three small workloads, every element ---------------------------------
+# n_splits None: the library's choice (split-KV for the two single-head
+# workloads); 1: the single-pass kernel.
+@pytest.mark.parametrize("n_splits", [None, 1])
 @pytest.mark.parametrize("name", ["single_head_256_d64", "single_head_4096_d64", "gpt2_small_causal_1024_d64"])
-def test_workload_elementwise(name):
-    _check_full(synth.WORKLOADS[name])
+def test_workload_elementwise(name, n_splits):
+    _check_full(synth.WORKLOADS[name], n_splits)
 
 
 # --- ragged and odd shapes, every element --------------------------------------
 RAGGED = [1, 2, 63, 65, 127, 129, 255, 257, 383, 1000]
 
 
+@pytest.mark.parametrize("n_splits", [None, 1])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("n", RAGGED)
-def test_ragged_square(n, d, causal):
-    _check_full(synth.Workload(f"ragged{n}", 1, 2, n, n, d, causal, seed=500 + n))
+def test_ragged_square(n, d, causal, n_splits):
+    _check_full(synth.Workload(f"ragged{n}", 1, 2, n, n, d, causal, seed=500 + n), n_splits)
+
+
+@pytest.mark.parametrize("n_splits", [None, 1])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("nq,nk", [(100, 300), (513, 64), (1, 1000), (256, 129), (700, 4097)])
+def test_rectangular_noncausal(nq, nk, d, n_splits):
+    _check_full(synth.Workload(f"rect{nq}x{nk}", 2, 1, nq, nk, d, False, seed=900 + nq), n_splits)
+
+
+# --- split-KV: forced slice counts, merge against the oracle ------------------
+@pytest.mark.parametrize("n_splits", [2, 3, 5, 16])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_splitkv_forced(n_splits, d, causal):
+    # 1000 keys = 8 K/V tiles (ragged tail): slices of 4, 3, 2 and 1 tiles; under
+    # the causal mask the light query tiles see only some slices (empty partials)
+    _check_full(synth.Workload("split", 2, 3, 1000, 1000, d, causal, seed=71), n_splits)
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("nq,nk", [(100, 300), (513, 64), (1, 1000), (256, 129), (700, 4097)])
-def test_rectangular_noncausal(nq, nk, d):
-    _check_full(synth.Workload(f"rect{nq}x{nk}", 2, 1, nq, nk, d, False, seed=900 + nq))
+def test_splitkv_wide_logits(d):
+    # the merge weights 2^(L_s - L) span many orders of magnitude
+    _check_full(synth.Workload("split_wide", 1, 2, 2000, 2000, d, True, sigma_q=20.0, seed=72), 7)
+
+
+def test_splitkv_workspace_errors():
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    q = torch.zeros((1, 1, 256, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 1, 256), dtype=torch.float32, device="cuda")
+    need = fa.fa_splitkv_workspace_bytes(1, 1, 256, 256, 64, 2)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = (q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 256, 256, 64, 0.125, 0, 2)
+    assert fa.fa_fwd_splitkv(*args, None, need, None) == 11
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need - 4, None) == 11
+    host_ws = torch.empty(need, dtype=torch.uint8)
+    assert fa.fa_fwd_splitkv(*args, host_ws.data_ptr(), need, None) == 10
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr() + 4, need, None) == 2
+    assert fa.fa_fwd_splitkv(*args, ws.data_ptr(), need, None) == 0
+    torch.cuda.synchronize()
 
 
 @pytest.mark.parametrize("d", [64, 128])
