@@ -15,7 +15,8 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "fa_fwd", "fa_fwd_splitkv", "fa_splitkv_workspace_bytes", "fa_splitkv_heuristic",
+__all__ = ["FaError", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
+           "fa_splitkv_heuristic", "NOALLOC_SCRATCH_BYTES",
            "fa_strerror", "fa_version", "fa_fwd_status", "fwd", "library_path", "load", "STATUS"]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -26,6 +27,8 @@ STATUS = {
     5: "FA_ERR_CAUSAL_SHAPE", 6: "FA_ERR_LAUNCH", 7: "FA_ERR_DEVICE", 8: "FA_ERR_TIMEOUT",
     9: "FA_ERR_SCALE", 10: "FA_ERR_POINTER", 11: "FA_ERR_WORKSPACE",
 }
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # FA_NOALLOC_SCRATCH_BYTES in include/fa.h
 
 _lib = None
 
@@ -64,6 +67,9 @@ def load():
         lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.fa_splitkv_heuristic.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.fa_splitkv_heuristic.restype = i32
+        lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                               i32, vp]
+        lib.fa_fwd_splitkv_noalloc.restype = i32
         _lib = lib
     return _lib
 
@@ -90,6 +96,17 @@ def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, wo
     """Raw C-ABI split-KV call; returns the status code (does not raise)."""
     return int(load().fa_fwd_splitkv(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
                                      int(causal), int(n_splits), workspace, int(workspace_bytes), stream))
+
+
+def fa_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, stream) -> int:
+    """Raw C-ABI split-KV call that allocates nothing (the library's fixed
+    device array holds the slice buffers); returns the status code.
+
+    For callers that cannot allocate device memory themselves.  Calls that
+    overlap on the GPU share that array and must be serialised by the caller.
+    """
+    return int(load().fa_fwd_splitkv_noalloc(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d),
+                                             float(scale), int(causal), int(n_splits), stream))
 
 
 def fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits) -> int:

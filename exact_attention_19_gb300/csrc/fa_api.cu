@@ -278,6 +278,53 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free split-KV.  For callers that may not allocate device memory
+// themselves (a host framework that owns the whole device pool, or a latency
+// path where a cudaMalloc and its implicit synchronisation are not allowed),
+// the slice buffers live in one fixed array in the library's own device
+// memory.  Each GPU that loads the library holds this array until the
+// process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+std::mutex g_noalloc_mutex;
+
+// The host-side name of a __device__ array is only a stand-in; the address a
+// kernel may use is asked of the runtime once per device, with that device
+// current.
+void* noalloc_scratch(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return g_noalloc_ptr[dev];
+}
+}  // namespace
+
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                           int Nk, int d, float scale, int causal, int n_splits, cudaStream_t stream) {
+  if (n_splits < 1 || n_splits > 64) return FA_ERR_SHAPE;
+  if (Nq > 0 && fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits) > FA_NOALLOC_SCRATCH_BYTES)
+    return FA_ERR_WORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
+  void* scratch = noalloc_scratch(dev);
+  if (!scratch) return FA_ERR_LAUNCH;
+  // Every partial the merge reads is written earlier in the same call (an
+  // empty slice writes weight 2^-inf), so nothing in the array has to be cleared.
+  return fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, scratch,
+                        FA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_LAUNCH;
   unsigned int word = 0;

@@ -111,6 +111,34 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_spl
  * each of at least two K/V tiles) to fill them about once. */
 int fa_splitkv_heuristic(int B, int H, int Nq, int Nk, int d, int causal);
 
+/* Size of the fixed device array fa_fwd_splitkv_noalloc works in. */
+#define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * fa_fwd_splitkv_noalloc -- fa_fwd_splitkv without a caller workspace and
+ * without any allocation: the slice buffers live in a fixed 16 MiB array
+ * (FA_NOALLOC_SCRATCH_BYTES) in the library's own device memory.  The pages
+ * describe no counterpart; this entry point exists for callers that cannot
+ * allocate device memory themselves, for instance code running inside a host
+ * framework that owns the whole device memory pool, or a latency path where a
+ * cudaMalloc and the synchronisation it implies are not allowed.
+ *
+ * Arguments and results as fa_fwd_splitkv.  Sizes whose workspace
+ * (fa_splitkv_workspace_bytes) exceeds FA_NOALLOC_SCRATCH_BYTES return
+ * FA_ERR_WORKSPACE before anything is launched.  No cudaMalloc, cudaFree or
+ * other allocating call is made.
+ * Every GPU that loads the library holds the array until the process exits.
+ * The first call on a device looks up the array's device address there (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the one array, which keeps whatever the last call left in
+ * it: calls whose kernels overlap on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller.  Nothing has to
+ * be cleared between calls: every value the merge reads is written earlier in
+ * the same call.
+ */
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                           int Nq, int Nk, int d, float scale, int causal, int n_splits, cudaStream_t stream);
+
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* fa_strerror(int status);
 

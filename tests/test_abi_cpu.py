@@ -101,3 +101,11 @@ def test_splitkv_host_validation(lib):
     assert st == 1
     st = fa.fa_fwd_splitkv(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 96, 0.125, 0, 2, FAKE, 1 << 20, None)
     assert st == 4
+
+
+def test_noalloc_host_validation(lib):
+    st = fa.fa_fwd_splitkv_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 128, 64, 0.125, 0, 0, None)
+    assert st == 3
+    # a request beyond the fixed array is refused before any device call
+    st = fa.fa_fwd_splitkv_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 4096, 4096, 128, 0.125, 0, 8, None)
+    assert st == 11
