@@ -57,6 +57,12 @@ def _declare(lib):
     lib.oracle_attention_rows.argtypes = [vp, vp, vp, ctypes.c_int, vp, i64, vp, vp, i64, i64, i64,
                                           i64, i64, ctypes.c_double, ctypes.c_int, ctypes.c_int]
     lib.oracle_attention_rows.restype = ctypes.c_int
+    lib.oracle_attention_fwd_window.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, i64, i64, i64, i64, i64,
+                                                ctypes.c_double, i64, i64, ctypes.c_int]
+    lib.oracle_attention_fwd_window.restype = ctypes.c_int
+    lib.oracle_attention_rows_window.argtypes = [vp, vp, vp, ctypes.c_int, vp, i64, vp, vp, i64, i64, i64,
+                                                 i64, i64, ctypes.c_double, i64, i64, ctypes.c_int]
+    lib.oracle_attention_rows_window.restype = ctypes.c_int
     lib.oracle_threads.argtypes = []
     lib.oracle_threads.restype = ctypes.c_int
     return lib
@@ -95,11 +101,13 @@ def _shapes(q, k, v):
     return B, H, Nq, k.shape[2], d
 
 
-def attention_fwd(q, k, v, scale, causal=False, nthreads=0, lib=None):
+def attention_fwd(q, k, v, scale, causal=False, nthreads=0, lib=None, window=None):
     """O [B,H,Nq,d] and LSE [B,H,Nq], both float64, for every query row.
 
     q, k, v: arrays [B, H, N, d] of float64, or of uint16 holding bf16 bits
-    (all three the same kind).
+    (all three the same kind).  window=(wl, wr): keep key j for row i iff
+    i + (Nk - Nq) - wl <= j <= i + (Nk - Nq) + wr, a negative bound meaning
+    unbounded (overrides ``causal``).
     """
     lib = lib or load_library()
     q, dq = _prep(q, "q")
@@ -110,6 +118,13 @@ def attention_fwd(q, k, v, scale, causal=False, nthreads=0, lib=None):
     B, H, Nq, Nk, d = _shapes(q, k, v)
     o = np.zeros((B, H, Nq, d), dtype=np.float64)
     lse = np.zeros((B, H, Nq), dtype=np.float64)
+    if window is not None:
+        rc = lib.oracle_attention_fwd_window(q.ctypes.data, k.ctypes.data, v.ctypes.data, dq, o.ctypes.data,
+                                             lse.ctypes.data, B, H, Nq, Nk, d, float(scale), int(window[0]),
+                                             int(window[1]), int(nthreads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attention_fwd_window failed ({rc})")
+        return o, lse
     rc = lib.oracle_attention_fwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dq, o.ctypes.data,
                                   lse.ctypes.data, B, H, Nq, Nk, d, float(scale), int(bool(causal)),
                                   int(nthreads))
@@ -118,10 +133,11 @@ def attention_fwd(q, k, v, scale, causal=False, nthreads=0, lib=None):
     return o, lse
 
 
-def attention_rows(q, k, v, rows, scale, causal=False, nthreads=0, lib=None):
+def attention_rows(q, k, v, rows, scale, causal=False, nthreads=0, lib=None, window=None):
     """O and LSE for selected query rows only.
 
     rows: flat indices (b*H + h)*Nq + i.  Returns o [len(rows), d], lse [len(rows)].
+    window as in ``attention_fwd``.
     """
     lib = lib or load_library()
     q, dq = _prep(q, "q")
@@ -133,6 +149,13 @@ def attention_rows(q, k, v, rows, scale, causal=False, nthreads=0, lib=None):
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     o = np.zeros((rows.size, d), dtype=np.float64)
     lse = np.zeros(rows.size, dtype=np.float64)
+    if window is not None:
+        rc = lib.oracle_attention_rows_window(q.ctypes.data, k.ctypes.data, v.ctypes.data, dq, rows.ctypes.data,
+                                              rows.size, o.ctypes.data, lse.ctypes.data, B, H, Nq, Nk, d,
+                                              float(scale), int(window[0]), int(window[1]), int(nthreads))
+        if rc != 0:
+            raise RuntimeError(f"oracle_attention_rows_window failed ({rc})")
+        return o, lse
     rc = lib.oracle_attention_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dq,
                                    rows.ctypes.data, rows.size, o.ctypes.data, lse.ctypes.data,
                                    B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(nthreads))

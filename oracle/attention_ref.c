@@ -26,10 +26,16 @@
  *   - causal masking keeps key j for query row i iff j <= i (top-left
  *     alignment); a masked key is left out of the row entirely, which is the
  *     same as exp(-inf) = 0;
+ *   - a sliding window (the "sliding" mask named beside "causal" in the
+ *     tiled loop of page "llm-infra-atlas / FlashAttention 01", section 3)
+ *     keeps key j for row i iff  i + s - wl <= j <= i + s + wr  with
+ *     s = Nk - Nq (the window's diagonal ends at the last query and the last
+ *     key: bottom-right alignment) and wl or wr < 0 meaning unbounded on that
+ *     side; causal is the window (-1, 0);
  *   - the scale multiplies the fp64 dot product (never a pre-scaled Q);
  *   - LSE is a natural logarithm, in scaled-logit units;
- *   - a row with no allowed key (impossible for valid causal shapes) gives
- *     O = 0 and LSE = -inf.
+ *   - a row with no allowed key (possible only under a window with Nq > Nk)
+ *     gives O = 0 and LSE = -inf.
  *
  * No tiling, no exp2, no online recurrence, no lazy rescaling: the sums run
  * over j in ascending order, in double precision.  bf16 inputs are widened to
@@ -68,10 +74,13 @@ static double load_elem(const void* base, int dtype, size_t idx) {
  */
 static void attend_one_row(const void* q, const void* k, const void* v, int dtype,
                            size_t q_base, size_t kv_base, long i, long Nk, long d,
-                           double scale, int causal, double* s_row, double* p_row,
+                           double scale, long j_first, long j_last, double* s_row, double* p_row,
                            double* o_row, double* lse_out) {
-  long n_keys = Nk;
-  if (causal && i + 1 < Nk) n_keys = i + 1; /* keys j <= i */
+  /* visible keys: j_first <= j <= j_last, clipped to [0, Nk) */
+  if (j_first < 0) j_first = 0;
+  if (j_last > Nk - 1) j_last = Nk - 1;
+  const long n_keys = j_last - j_first + 1;
+  (void)i;
 
   for (long c = 0; c < d; ++c) o_row[c] = 0.0;
   if (n_keys <= 0) {
@@ -79,33 +88,48 @@ static void attend_one_row(const void* q, const void* k, const void* v, int dtyp
     return;
   }
 
-  /* S row: s_j = scale * <q_i, k_j> */
-  for (long j = 0; j < n_keys; ++j) {
+  /* S row: s_j = scale * <q_i, k_j>, stored at index j - j_first */
+  for (long j = j_first; j <= j_last; ++j) {
     double dot = 0.0;
     size_t krow = kv_base + (size_t)j * (size_t)d;
     for (long c = 0; c < d; ++c)
       dot += load_elem(q, dtype, q_base + (size_t)c) * load_elem(k, dtype, krow + (size_t)c);
-    s_row[j] = scale * dot;
+    s_row[j - j_first] = scale * dot;
   }
 
   /* safe softmax: pass 1 max, pass 2 sum of exp(s - m), pass 3 normalise */
   double m = s_row[0];
-  for (long j = 1; j < n_keys; ++j)
-    if (s_row[j] > m) m = s_row[j];
+  for (long t = 1; t < n_keys; ++t)
+    if (s_row[t] > m) m = s_row[t];
   double l = 0.0;
-  for (long j = 0; j < n_keys; ++j) {
-    p_row[j] = exp(s_row[j] - m);
-    l += p_row[j];
+  for (long t = 0; t < n_keys; ++t) {
+    p_row[t] = exp(s_row[t] - m);
+    l += p_row[t];
   }
-  for (long j = 0; j < n_keys; ++j) p_row[j] = p_row[j] / l;
+  for (long t = 0; t < n_keys; ++t) p_row[t] = p_row[t] / l;
 
   /* O row = P row times V */
-  for (long j = 0; j < n_keys; ++j) {
-    size_t vrow = kv_base + (size_t)j * (size_t)d;
-    double pj = p_row[j];
+  for (long t = 0; t < n_keys; ++t) {
+    size_t vrow = kv_base + (size_t)(j_first + t) * (size_t)d;
+    double pj = p_row[t];
     for (long c = 0; c < d; ++c) o_row[c] += pj * load_elem(v, dtype, vrow + (size_t)c);
   }
   *lse_out = m + log(l);
+}
+
+/* Visible key range of row i.  mode 0: all keys; mode 1: causal, top-left
+ * (j <= i); mode 2: window (wl, wr), bottom-right aligned. */
+static void key_range(long i, long Nq, long Nk, int mode, long long wl, long long wr, long* j_first,
+                      long* j_last) {
+  *j_first = 0;
+  *j_last = Nk - 1;
+  if (mode == 1) {
+    *j_last = i;
+  } else if (mode == 2) {
+    const long long diag = (long long)i + (long long)Nk - (long long)Nq;
+    if (wl >= 0) *j_first = (long)(diag - wl > -1 ? diag - wl : -1);
+    if (wr >= 0) *j_last = (long)(diag + wr < (long long)Nk ? diag + wr : (long long)Nk);
+  }
 }
 
 int oracle_threads(void) {
@@ -122,10 +146,31 @@ int oracle_threads(void) {
  * Inputs laid out [B, H, Nq, d] (q) and [B, H, Nk, d] (k, v), contiguous.
  * Returns 0 on success, a negative value on bad arguments or no memory.
  */
+static int rows_impl(const void* q, const void* k, const void* v, int dtype, const long long* rows,
+                     long long n_rows, double* o, double* lse, long long B, long long H, long long Nq,
+                     long long Nk, long long d, double scale, int mode, long long wl, long long wr,
+                     int nthreads);
+
 int oracle_attention_rows(const void* q, const void* k, const void* v, int dtype,
                           const long long* rows, long long n_rows, double* o, double* lse,
                           long long B, long long H, long long Nq, long long Nk, long long d,
                           double scale, int causal, int nthreads) {
+  return rows_impl(q, k, v, dtype, rows, n_rows, o, lse, B, H, Nq, Nk, d, scale, causal ? 1 : 0, -1, -1,
+                   nthreads);
+}
+
+/* Selected rows under a window (wl, wr) aligned bottom-right; < 0 = unbounded. */
+int oracle_attention_rows_window(const void* q, const void* k, const void* v, int dtype,
+                                 const long long* rows, long long n_rows, double* o, double* lse,
+                                 long long B, long long H, long long Nq, long long Nk, long long d,
+                                 double scale, long long wl, long long wr, int nthreads) {
+  return rows_impl(q, k, v, dtype, rows, n_rows, o, lse, B, H, Nq, Nk, d, scale, 2, wl, wr, nthreads);
+}
+
+static int rows_impl(const void* q, const void* k, const void* v, int dtype, const long long* rows,
+                     long long n_rows, double* o, double* lse, long long B, long long H, long long Nq,
+                     long long Nk, long long d, double scale, int mode, long long wl, long long wr,
+                     int nthreads) {
   if (!q || !k || !v || !o || !lse || (!rows && n_rows > 0)) return -1;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0 || n_rows < 0) return -2;
   if (dtype != ORACLE_F64 && dtype != ORACLE_BF16) return -3;
@@ -154,7 +199,9 @@ int oracle_attention_rows(const void* q, const void* k, const void* v, int dtype
         long long i = flat % Nq;
         size_t q_base = (size_t)flat * (size_t)d;
         size_t kv_base = (size_t)bh * (size_t)Nk * (size_t)d;
-        attend_one_row(q, k, v, dtype, q_base, kv_base, (long)i, (long)Nk, (long)d, scale, causal,
+        long jf, jl;
+        key_range((long)i, (long)Nq, (long)Nk, mode, wl, wr, &jf, &jl);
+        attend_one_row(q, k, v, dtype, q_base, kv_base, (long)i, (long)Nk, (long)d, scale, jf, jl,
                        s_row, p_row, o + (size_t)r * (size_t)d, lse + r);
       }
     }
@@ -164,10 +211,27 @@ int oracle_attention_rows(const void* q, const void* k, const void* v, int dtype
   return failed ? -5 : 0;
 }
 
+static int fwd_impl(const void* q, const void* k, const void* v, int dtype, double* o, double* lse,
+                    long long B, long long H, long long Nq, long long Nk, long long d, double scale,
+                    int mode, long long wl, long long wr, int nthreads);
+
 /* All rows: o[B*H*Nq*d], lse[B*H*Nq]. */
 int oracle_attention_fwd(const void* q, const void* k, const void* v, int dtype, double* o,
                          double* lse, long long B, long long H, long long Nq, long long Nk,
                          long long d, double scale, int causal, int nthreads) {
+  return fwd_impl(q, k, v, dtype, o, lse, B, H, Nq, Nk, d, scale, causal ? 1 : 0, -1, -1, nthreads);
+}
+
+/* All rows under a window (wl, wr) aligned bottom-right; < 0 = unbounded. */
+int oracle_attention_fwd_window(const void* q, const void* k, const void* v, int dtype, double* o,
+                                double* lse, long long B, long long H, long long Nq, long long Nk,
+                                long long d, double scale, long long wl, long long wr, int nthreads) {
+  return fwd_impl(q, k, v, dtype, o, lse, B, H, Nq, Nk, d, scale, 2, wl, wr, nthreads);
+}
+
+static int fwd_impl(const void* q, const void* k, const void* v, int dtype, double* o, double* lse,
+                    long long B, long long H, long long Nq, long long Nk, long long d, double scale,
+                    int mode, long long wl, long long wr, int nthreads) {
   if (!q || !k || !v || !o || !lse) return -1;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return -2;
   if (dtype != ORACLE_F64 && dtype != ORACLE_BF16) return -3;
@@ -193,7 +257,9 @@ int oracle_attention_fwd(const void* q, const void* k, const void* v, int dtype,
         long long i = flat % Nq;
         size_t q_base = (size_t)flat * (size_t)d;
         size_t kv_base = (size_t)bh * (size_t)Nk * (size_t)d;
-        attend_one_row(q, k, v, dtype, q_base, kv_base, (long)i, (long)Nk, (long)d, scale, causal,
+        long jf, jl;
+        key_range((long)i, (long)Nq, (long)Nk, mode, wl, wr, &jf, &jl);
+        attend_one_row(q, k, v, dtype, q_base, kv_base, (long)i, (long)Nk, (long)d, scale, jf, jl,
                        s_row, p_row, o + (size_t)flat * (size_t)d, lse + flat);
       }
     }

@@ -372,3 +372,76 @@ PINS = [
     pin_closed_forms, pin_shift_invariance, pin_permutation_invariance, pin_batch_head_layout,
     pin_torch_softmax, pin_sim_cases, pin_brute_force, pin_bf16_inputs,
 ]
+
+
+# ---------------------------------------------------------------------------
+# window masks (bottom-right aligned sliding window; causal = (-1, 0))
+# ---------------------------------------------------------------------------
+def _brute_window(q, k, v, scale, wl, wr):
+    """Direct loop: key j kept for row i iff i+s-wl <= j <= i+s+wr, s = Nk - Nq."""
+    nq, nk, d = len(q), len(k), len(q[0])
+    s = nk - nq
+    o = [[0.0] * d for _ in range(nq)]
+    lse = [0.0] * nq
+    for i in range(nq):
+        keys = [j for j in range(nk) if (wl < 0 or j >= i + s - wl) and (wr < 0 or j <= i + s + wr)]
+        if not keys:
+            lse[i] = -math.inf
+            continue
+        w = [math.exp(scale * sum(q[i][c] * k[j][c] for c in range(d))) for j in keys]
+        z = sum(w)
+        for c in range(d):
+            o[i][c] = sum(wj * v[j][c] for wj, j in zip(w, keys)) / z
+        lse[i] = math.log(z)
+    return o, lse
+
+
+def pin_window_brute_force(lib):
+    rng = _rng(31)
+    for (nq, nk) in [(5, 5), (3, 8), (8, 3), (1, 6), (7, 1)]:
+        for (wl, wr) in [(-1, 0), (0, 0), (2, 1), (1, -1), (-1, -1), (0, 3), (4, 0)]:
+            q = rng.normal(size=(nq, 3))
+            k = rng.normal(size=(nk, 3))
+            v = rng.normal(size=(nk, 3))
+            ob, lb = _brute_window(q.tolist(), k.tolist(), v.tolist(), 0.8, wl, wr)
+            o, lse = oracle.attention_fwd(*_one_head(q, k, v), scale=0.8, window=(wl, wr), lib=lib)
+            lb = np.array(lb)
+            fin = np.isfinite(lb)
+            assert np.array_equal(np.isfinite(lse[0, 0]), fin), (nq, nk, wl, wr)
+            assert np.max(np.abs(lse[0, 0][fin] - lb[fin]), initial=0.0) < 1e-12, (nq, nk, wl, wr)
+            assert np.max(np.abs(o[0, 0] - np.array(ob))) < 1e-12, (nq, nk, wl, wr)
+            # rows without a visible key: O = 0 exactly
+            assert np.all(o[0, 0][~fin] == 0.0)
+
+
+def pin_window_special_cases(lib):
+    rng = _rng(32)
+    n, d = 20, 4
+    q = rng.normal(size=(n, d))
+    k = rng.normal(size=(n, d))
+    v = rng.normal(size=(n, d))
+    # unbounded on both sides = no mask; (-1, 0) with Nq = Nk = causal
+    o0, l0 = oracle.attention_fwd(*_one_head(q, k, v), scale=0.5, lib=lib)
+    o1, l1 = oracle.attention_fwd(*_one_head(q, k, v), scale=0.5, window=(-1, -1), lib=lib)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    o0, l0 = oracle.attention_fwd(*_one_head(q, k, v), scale=0.5, causal=True, lib=lib)
+    o1, l1 = oracle.attention_fwd(*_one_head(q, k, v), scale=0.5, window=(-1, 0), lib=lib)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    # K = 0 under a window: uniform weights over the visible keys
+    nq, nk, wl, wr = 6, 10, 2, 1
+    qz = rng.normal(size=(nq, d))
+    vz = rng.normal(size=(nk, d))
+    o, lse = oracle.attention_fwd(*_one_head(qz, np.zeros((nk, d)), vz), scale=1.0, window=(wl, wr), lib=lib)
+    for i in range(nq):
+        lo = max(0, i + (nk - nq) - wl)
+        hi = min(nk - 1, i + (nk - nq) + wr)
+        assert abs(lse[0, 0, i] - math.log(hi - lo + 1)) < 1e-14
+        assert np.max(np.abs(o[0, 0, i] - vz[lo:hi + 1].mean(axis=0))) < 1e-14
+    # selected-rows entry agrees with the all-rows entry
+    rows = np.array([0, 3, 5])
+    orow, lrow = oracle.attention_rows(*_one_head(qz, np.zeros((nk, d)), vz), rows, scale=1.0, window=(wl, wr),
+                                       lib=lib)
+    assert np.array_equal(orow, o.reshape(-1, d)[rows]) and np.array_equal(lrow, lse.reshape(-1)[rows])
+
+
+PINS += [pin_window_brute_force, pin_window_special_cases]
