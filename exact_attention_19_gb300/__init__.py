@@ -15,7 +15,7 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "fa_fwd", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
+__all__ = ["FaError", "fa_fwd", "fa_fwd_window", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
            "fa_splitkv_heuristic", "NOALLOC_SCRATCH_BYTES",
            "fa_strerror", "fa_version", "fa_fwd_status", "fwd", "library_path", "load", "STATUS"]
 
@@ -70,6 +70,8 @@ def load():
         lib.fa_fwd_splitkv_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
                                                i32, vp]
         lib.fa_fwd_splitkv_noalloc.restype = i32
+        lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp]
+        lib.fa_fwd_window.restype = i32
         _lib = lib
     return _lib
 
@@ -89,6 +91,12 @@ def fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream) -> int:
     """
     return int(load().fa_fwd(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
                              int(causal), stream))
+
+
+def fa_fwd_window(q, k, v, o, lse, B, H, Nq, Nk, d, scale, window_left, window_right, stream) -> int:
+    """Raw C-ABI sliding-window call (bottom-right aligned, -1 = unbounded); returns the status code."""
+    return int(load().fa_fwd_window(q, k, v, o, lse, int(B), int(H), int(Nq), int(Nk), int(d), float(scale),
+                                    int(window_left), int(window_right), stream))
 
 
 def fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, workspace, workspace_bytes,
@@ -133,7 +141,7 @@ def _stream_handle(stream):
 
 
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, stream=None,
-        n_splits: int | None = None, workspace=None):
+        n_splits: int | None = None, workspace=None, window: tuple | None = None):
     """O = softmax(q k^T * scale) v and the per-row LSE, on the GPU.
 
     q: [B, H, Nq, d], k, v: [B, H, Nk, d] torch.bfloat16 CUDA tensors,
@@ -145,6 +153,10 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     query tiles to fill the GPU); None asks the library's heuristic, 1 forces
     the single-pass kernel.  ``workspace`` (a CUDA tensor of at least
     ``fa_splitkv_workspace_bytes`` bytes) may be given to avoid allocating it.
+
+    ``window=(left, right)``: sliding-window mask aligned bottom-right (key j
+    visible to row i iff i+Nk-Nq-left <= j <= i+Nk-Nq+right, -1 = unbounded);
+    replaces ``causal`` and runs the single-pass kernel.
     """
     import torch
 
@@ -167,6 +179,12 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
         raise ValueError("out must be a contiguous bf16 tensor shaped like q")
     if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    if window is not None:
+        st = fa_fwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Nq, Nk,
+                           d, scale, int(window[0]), int(window[1]), _stream_handle(stream))
+        if st != 0:
+            raise FaError(st, "fa_fwd_window")
+        return out, lse
     if n_splits is None:
         n_splits = fa_splitkv_heuristic(B, H, Nq, Nk, d, int(bool(causal))) if Nq > 0 else 1
     if n_splits > 1:

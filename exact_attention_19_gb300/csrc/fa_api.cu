@@ -46,10 +46,19 @@ int g_dev_sms_or(int dev, int fallback) {
 }
 std::mutex g_dev_mutex;
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, int MASK, bool SPLIT>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, CAUSAL, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, MASK, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::Cfg<D>::kSmemBytes));
+}
+
+template <int D>
+bool set_smem_attrs() {
+  return set_smem_attr<D, fa::kMaskNone, false>() == cudaSuccess &&
+         set_smem_attr<D, fa::kMaskCausal, false>() == cudaSuccess &&
+         set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
+         set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
+         set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
 }
 
 int prepare_device(int dev) {
@@ -72,11 +81,7 @@ int prepare_device(int dev) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return FA_ERR_LAUNCH;
   g_dev_sms[dev] = sms;
-  if (set_smem_attr<64, false, false>() != cudaSuccess || set_smem_attr<64, true, false>() != cudaSuccess ||
-      set_smem_attr<128, false, false>() != cudaSuccess || set_smem_attr<128, true, false>() != cudaSuccess ||
-      set_smem_attr<64, false, true>() != cudaSuccess || set_smem_attr<64, true, true>() != cudaSuccess ||
-      set_smem_attr<128, false, true>() != cudaSuccess || set_smem_attr<128, true, true>() != cudaSuccess)
-    return FA_ERR_LAUNCH;
+  if (!set_smem_attrs<64>() || !set_smem_attrs<128>()) return FA_ERR_LAUNCH;
   g_dev_state[dev].store(1, std::memory_order_release);
   return FA_OK;
 }
@@ -106,19 +111,20 @@ bool make_map(CUtensorMap* map, const void* ptr, int D, long long N, long long B
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, int MASK, bool SPLIT>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
            long long grid, cudaStream_t stream) {
-  fa::fa_fwd_kernel<D, CAUSAL, SPLIT><<<static_cast<unsigned>(grid), fa::Cfg<D>::kThreads,
-                                        fa::Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  fa::fa_fwd_kernel<D, MASK, SPLIT><<<static_cast<unsigned>(grid), fa::Cfg<D>::kThreads,
+                                      fa::Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
+// no mask or the causal mask (split or not)
 template <int D, bool SPLIT>
 int launch_d(bool causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
              const fa::FwdParams& p, long long grid, cudaStream_t stream) {
-  return causal ? launch<D, true, SPLIT>(mq, mk, mv, p, grid, stream)
-                : launch<D, false, SPLIT>(mq, mk, mv, p, grid, stream);
+  return causal ? launch<D, fa::kMaskCausal, SPLIT>(mq, mk, mv, p, grid, stream)
+                : launch<D, fa::kMaskNone, SPLIT>(mq, mk, mv, p, grid, stream);
 }
 
 // Checks shared by fa_fwd and fa_fwd_splitkv.  On success fills the tensor
@@ -162,6 +168,10 @@ int prepare_call(const void* q, const void* k, const void* v, void* o, float* ls
   p->Nk = Nk;
   p->n_pairs = static_cast<int>(n_pairs);
   p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  // causal = the window (-1, 0) on the main diagonal (Nq == Nk here)
+  p->win_left = -1;
+  p->win_right = causal ? 0 : -1;
+  p->diag_off = 0;
   p->n_splits = 1;
   p->split_tiles = 0;
   p->o_part = nullptr;
@@ -214,6 +224,26 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   const long long grid = static_cast<long long>(B) * H * p.n_pairs;
   return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, p, grid, stream)
                  : launch_d<128, false>(causal, mq, mk, mv, p, grid, stream);
+}
+
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                  int Nk, int d, float scale, int window_left, int window_right, cudaStream_t stream) {
+  if (window_left < -1 || window_right < -1) return FA_ERR_SHAPE;
+  CUtensorMap mq, mk, mv;
+  fa::FwdParams p;
+  int dev = -1;
+  bool noop = false;
+  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, 0, &mq, &mk, &mv, &p, &dev, &noop);
+  if (st != FA_OK || noop) return st;
+  p.win_left = window_left;
+  p.win_right = window_right;
+  p.diag_off = Nk - Nq;  // bottom-right: the window's diagonal ends at (Nq - 1, Nk - 1)
+  const long long grid = static_cast<long long>(B) * H * p.n_pairs;
+  if (window_left < 0 && window_right < 0)  // no bound on either side: no mask
+    return d == 64 ? launch<64, fa::kMaskNone, false>(mq, mk, mv, p, grid, stream)
+                   : launch<128, fa::kMaskNone, false>(mq, mk, mv, p, grid, stream);
+  return d == 64 ? launch<64, fa::kMaskWindow, false>(mq, mk, mv, p, grid, stream)
+                 : launch<128, fa::kMaskWindow, false>(mq, mk, mv, p, grid, stream);
 }
 
 size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_splits) {

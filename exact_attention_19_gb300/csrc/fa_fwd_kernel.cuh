@@ -46,6 +46,9 @@ struct FwdParams {
   int Nq, Nk;
   int n_pairs;        // ceil(Nq / 256): query-tile pairs per (b, h)
   float scale_log2;   // scale * log2(e)
+  // MASKED only: key j is visible to query row i iff
+  //   i + diag_off - win_left <= j <= i + diag_off + win_right  (a negative bound: unbounded)
+  int win_left, win_right, diag_off;
   // split-KV only: CTAs per pair, K/V tiles per split, and the partial results
   int n_splits, split_tiles;
   float* o_part;      // fp32 [n_splits, BH * Nq, D], each slice normalised by its own l
@@ -85,9 +88,16 @@ __device__ __forceinline__ void report_wait_failure(volatile int* abort, unsigne
   atomicOr(&g_fa_status, 1u | (role << 8));
 }
 
+// MASK: kMaskNone, kMaskCausal (key j visible to row i iff j <= i, Nq == Nk)
+// or kMaskWindow (the general window of FwdParams); each query tile visits
+// only the K/V tiles its rows can see and masks the partly visible ones.  The
+// causal case is the window (-1, 0) with diag_off 0, specialised at compile
+// time so that its bounds fold to constants.
 // SPLIT: the CTA covers K/V tiles [split * split_tiles, (split+1) * split_tiles)
 // of its pair and writes a partial result; fa_splitkv_combine_kernel merges them.
-template <int D, bool CAUSAL, bool SPLIT>
+enum : int { kMaskNone = 0, kMaskCausal = 1, kMaskWindow = 2 };
+
+template <int D, int MASK, bool SPLIT>
 __global__ void __launch_bounds__(320, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -143,18 +153,49 @@ __global__ void __launch_bounds__(320, 1)
   }
   const int bh = cta / p.n_pairs;
   int pair = cta % p.n_pairs;
-  if (CAUSAL) pair = p.n_pairs - 1 - pair;  // heaviest pair of each head first
+  constexpr bool MASKED = MASK != kMaskNone;
+  if (MASK == kMaskCausal) pair = p.n_pairs - 1 - pair;  // heaviest pair of each head first
   const int n_kv_all = (p.Nk + C::kBN - 1) / C::kBN;
-  const int kv_lo = SPLIT ? split * p.split_tiles : 0;  // first K/V tile of this CTA
-  int row0[2], nkv[2], nkv_full[2];
+  const int kv_lo = SPLIT ? split * p.split_tiles : 0;  // this CTA's slice of K/V tiles
+  const int kv_hi = SPLIT ? min(n_kv_all, kv_lo + p.split_tiles) : n_kv_all;
+  // visible K/V tiles [jlo, jhi) of each query tile, within the slice
+  int row0[2], jlo[2], jhi[2], nkv[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int qt = 2 * pair + t;
     row0[t] = qt * C::kBM;
-    nkv_full[t] = (row0[t] < p.Nq) ? (CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all) : 0;
-    nkv[t] = SPLIT ? max(0, min(nkv_full[t], kv_lo + p.split_tiles) - kv_lo) : nkv_full[t];
+    int lo = 0, hi = 0;
+    if (row0[t] < p.Nq) {
+      hi = n_kv_all;
+      if (MASK == kMaskCausal) {
+        hi = min(n_kv_all, qt + 1);
+      } else if (MASK == kMaskWindow) {
+        const long long r_first = row0[t], r_last = min(row0[t] + C::kBM, p.Nq) - 1;
+        long long key_lo = 0, key_hi = p.Nk - 1;
+        if (p.win_left >= 0) key_lo = max(0ll, r_first + p.diag_off - p.win_left);
+        if (p.win_right >= 0) key_hi = min(key_hi, r_last + p.diag_off + p.win_right);
+        if (key_lo > key_hi) {
+          hi = 0;  // no row of this tile sees a key
+        } else {
+          lo = static_cast<int>(key_lo / C::kBN);
+          hi = static_cast<int>(key_hi / C::kBN) + 1;
+        }
+      }
+      lo = max(lo, kv_lo);
+      hi = min(hi, kv_hi);
+      if (hi < lo) hi = lo;
+    }
+    jlo[t] = lo;
+    jhi[t] = hi;
+    nkv[t] = hi - lo;
   }
-  const int n_max = max(nkv[0], nkv[1]);
+  // the CTA streams the union of the two ranges: K/V tiles [J0, J0 + n_max)
+  int J0 = 0, n_max = 0;
+  if (nkv[0] > 0 || nkv[1] > 0) {
+    J0 = nkv[0] == 0 ? jlo[1] : (nkv[1] == 0 ? jlo[0] : min(jlo[0], jlo[1]));
+    const int J1 = nkv[0] == 0 ? jhi[1] : (nkv[1] == 0 ? jhi[0] : max(jhi[0], jhi[1]));
+    n_max = J1 - J0;
+  }
   const int n_items = 2 * n_max;  // ring items: K_j = item 2j, V_j = item 2j+1
 
   if (warp == 8) {
@@ -181,8 +222,7 @@ __global__ void __launch_bounds__(320, 1)
         const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
         mbar_arrive_expect_tx(full(s), C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (kv_lo + (item >> 1)) * C::kBN,
-                      bh);
+          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (J0 + (item >> 1)) * C::kBN, bh);
         issued = item + 1;
       }
       if (*abort_flag) {
@@ -223,6 +263,8 @@ __global__ void __launch_bounds__(320, 1)
       auto wait_item = [&](int item) -> bool {
         return mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, abort_flag);
       };
+      // is K/V tile j (absolute index within the head) visible to query tile t?
+      auto in_range = [&](int t, int j) -> bool { return j >= jlo[t] && j < jhi[t]; };
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
         if (nkv[t] > 0) ok = mbar_wait(bar(kBarQ + t), 0, abort_flag);
@@ -230,7 +272,7 @@ __global__ void __launch_bounds__(320, 1)
       if (ok && n_max > 0) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
-          if (nkv[t] > 0) {
+          if (nkv[t] > 0 && jlo[t] == J0) {
             gemm1(t, 0);
             mma_commit(bar(kBarS + t));
           }
@@ -239,38 +281,41 @@ __global__ void __launch_bounds__(320, 1)
       // Issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), with
       // every barrier check of the first half gathered in one place (each
       // check behind queued MMAs costs a pipe bubble, consecutive ones cost one).
-      for (int j = 0; ok && j < n_max; ++j) {
-        const int iv = 2 * j + 1, ik = 2 * j + 2;  // ring items of V_j and K_{j+1}
+      // A tile whose range starts after J0 gets its first S when j + 1 enters it.
+      for (int jj = 0; ok && jj < n_max; ++jj) {
+        const int j = J0 + jj;
+        const int iv = 2 * jj + 1, ik = 2 * jj + 2;  // ring items of V_j and K_{j+1}
         const int sv = iv % C::kRing, sk = ik % C::kRing;
-        const bool has_next = (j + 1) < n_max;
+        const bool has_next = (jj + 1) < n_max;
+        const bool pv0 = in_range(0, j), pv1 = in_range(1, j);
         {
           // the three checks are issued back to back so their latencies overlap
           const bool a = mbar_try_wait(full(sv), (iv / C::kRing) & 1);
           const bool b = !has_next || mbar_try_wait(full(sk), (ik / C::kRing) & 1);
-          const bool c = j >= nkv[0] || mbar_try_wait(bar(kBarP + 0), j & 1);
+          const bool c = !pv0 || mbar_try_wait(bar(kBarP + 0), (j - jlo[0]) & 1);
           if (!(a && b && c)) {
             if (!(ok = wait_item(iv))) break;
             if (has_next && !(ok = wait_item(ik))) break;
-            if (j < nkv[0] && !(ok = mbar_wait(bar(kBarP + 0), j & 1, abort_flag))) break;
+            if (pv0 && !(ok = mbar_wait(bar(kBarP + 0), (j - jlo[0]) & 1, abort_flag))) break;
           }
         }
         tc_fence_after();
-        if (j < nkv[0]) {
-          gemm2(0, sv, j > 0);
-          if (j == nkv[0] - 1) mma_commit(bar(kBarO + 0));
+        if (pv0) {
+          gemm2(0, sv, j > jlo[0]);
+          if (j == jhi[0] - 1) mma_commit(bar(kBarO + 0));
         }
-        if (j + 1 < nkv[0]) {
+        if (has_next && in_range(0, j + 1)) {
           gemm1(0, sk);
           mma_commit(bar(kBarS + 0));
         }
-        if (j < nkv[1]) {
-          if (!(ok = mbar_wait(bar(kBarP + 1), j & 1, abort_flag))) break;
+        if (pv1) {
+          if (!(ok = mbar_wait(bar(kBarP + 1), (j - jlo[1]) & 1, abort_flag))) break;
           tc_fence_after();
-          gemm2(1, sv, j > 0);
-          if (j == nkv[1] - 1) mma_commit(bar(kBarO + 1));
+          gemm2(1, sv, j > jlo[1]);
+          if (j == jhi[1] - 1) mma_commit(bar(kBarO + 1));
         }
         mma_commit(empty(sv));
-        if (j + 1 < nkv[1]) {
+        if (has_next && in_range(1, j + 1)) {
           gemm1(1, sk);
           mma_commit(bar(kBarS + 1));
         }
@@ -287,6 +332,17 @@ __global__ void __launch_bounds__(320, 1)
     const int wq = warp & 3;        // TMEM lane quarter
     const int row_local = wq * 32 + lane;
     const int row = row0[t] + row_local;
+    // keys [row_key_lo, row_key_end) are visible to this row; all sizes fit
+    // an int (N < 2^31), the window bounds are clamped into [-1, Nk]
+    int row_key_lo = 0, row_key_end = p.Nk;
+    if (MASK == kMaskCausal) row_key_end = min(p.Nk, row + 1);
+    if (MASK == kMaskWindow) {
+      if (p.win_left >= 0)
+        row_key_lo = static_cast<int>(max(-1ll, static_cast<long long>(row) + p.diag_off - p.win_left));
+      if (p.win_right >= 0)
+        row_key_end = static_cast<int>(
+            min(static_cast<long long>(p.Nk), max(-1ll, static_cast<long long>(row) + p.diag_off + p.win_right) + 1));
+    }
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t tS = lane_base + (t == 0 ? C::kTmS0 : C::kTmS1);
     const uint32_t tO = lane_base + (t == 0 ? C::kTmO0 : C::kTmO1);
@@ -315,19 +371,17 @@ __global__ void __launch_bounds__(320, 1)
       float* const f2 = reinterpret_cast<float*>(s2);
       float* const f3 = reinterpret_cast<float*>(s3);
 
-      // masking: ragged key tail and the causal diagonal tile
-      const int jg = kv_lo + j;  // K/V tile index within the head
-      const bool tail = (jg == n_kv_all - 1) && (p.Nk % C::kBN != 0);
-      const bool diag = CAUSAL && (jg == nkv_full[t] - 1);
-      const bool masked = tail || diag;
-      int lim = p.Nk;
-      if (CAUSAL) lim = min(lim, row + 1);
-      lim -= jg * C::kBN;  // columns >= lim are masked
+      // masking: columns outside [lim_lo, lim_hi) of this K/V tile are not
+      // visible to this row (window / causal bounds, ragged key tail)
+      const int k0 = (jlo[t] + j) * C::kBN;  // first key of this K/V tile
+      const int lim_lo = MASK == kMaskWindow ? min(C::kBN, max(0, row_key_lo - k0)) : 0;
+      const int lim_hi = min(C::kBN, max(0, row_key_end - k0));
+      const bool masked = lim_lo > 0 || lim_hi < C::kBN;
       if (masked) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (i >= lim) f0[i] = NEG_INF;
-          if (32 + i >= lim) f1[i] = NEG_INF;
+          if (i < lim_lo || i >= lim_hi) f0[i] = NEG_INF;
+          if (32 + i < lim_lo || 32 + i >= lim_hi) f1[i] = NEG_INF;
         }
       }
       float mx0 = fmax3(f0[0], f0[1], f1[0]), mx1 = fmax3(f0[2], f0[3], f1[1]);
@@ -343,8 +397,8 @@ __global__ void __launch_bounds__(320, 1)
       if (masked) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (64 + i >= lim) f2[i] = NEG_INF;
-          if (96 + i >= lim) f3[i] = NEG_INF;
+          if (64 + i < lim_lo || 64 + i >= lim_hi) f2[i] = NEG_INF;
+          if (96 + i < lim_lo || 96 + i >= lim_hi) f3[i] = NEG_INF;
         }
       }
       float mx2 = fmax3(f2[0], f2[1], f3[0]), mx3 = fmax3(f2[2], f2[3], f3[1]);
@@ -456,6 +510,13 @@ __global__ void __launch_bounds__(320, 1)
           if (store) p.lse_part[prow] = (l > 0.f) ? (m_bar + __log2f(l)) : NEG_INF;
         }
       }
+    } else if (!SPLIT && ok && nt == 0 && row < p.Nq) {
+      // no row of this tile sees a key (possible under a window): O = 0, LSE = -inf
+      uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                   (static_cast<size_t>(bh) * p.Nq + row) * D);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) orow[i] = make_uint4(0u, 0u, 0u, 0u);
+      p.lse[static_cast<size_t>(bh) * p.Nq + row] = NEG_INF;
     } else if (SPLIT && ok && nt == 0 && row < p.Nq) {
       // no visible key in this slice: an empty partial (weight 2^-inf = 0)
       const size_t prow = static_cast<size_t>(split) * p.rows + static_cast<size_t>(bh) * p.Nq + row;

@@ -76,6 +76,24 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
            int Nk, int d, float scale, int causal, cudaStream_t stream);
 
 /*
+ * fa_fwd_window -- fa_fwd under a sliding-window mask (the "sliding" mask that
+ * "llm-infra-atlas / FlashAttention 01", section 3, names beside "causal" in
+ * the tiled loop; the window form and its alignment are this library's
+ * reading, the pages give no formula).
+ *
+ * Key j is visible to query row i iff
+ *     i + (Nk - Nq) - window_left  <=  j  <=  i + (Nk - Nq) + window_right,
+ * i.e. the window is aligned so that its diagonal ends at the last query and
+ * the last key (bottom-right alignment); -1 leaves that side unbounded.
+ * (-1, 0) is causal attention for any Nq and Nk; (-1, -1) is no mask.  A query
+ * row that sees no key gets O = 0 and LSE = -inf.
+ * Arguments otherwise as fa_fwd (no causal flag, Nq and Nk independent);
+ * window_left or window_right below -1 returns FA_ERR_SHAPE.
+ */
+int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                  int Nk, int d, float scale, int window_left, int window_right, cudaStream_t stream);
+
+/*
  * fa_fwd_splitkv -- the same operation as fa_fwd, with each query tile's K/V
  * range cut into n_splits slices processed by separate CTAs, for shapes whose
  * B * H * ceil(Nq / 256) CTAs would leave most of the GPU idle.

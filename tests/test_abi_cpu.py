@@ -109,3 +109,10 @@ def test_noalloc_host_validation(lib):
     # a request beyond the fixed array is refused before any device call
     st = fa.fa_fwd_splitkv_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 4096, 4096, 128, 0.125, 0, 8, None)
     assert st == 11
+
+
+def test_window_host_validation(lib):
+    assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 64, 0.125, -2, 0, None) == 3
+    assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 64, 0.125, 0, -5, None) == 3
+    assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 96, 0.125, 0, 0, None) == 4
+    assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 0, 256, 64, 0.125, 10, 0, None) == 0

@@ -247,3 +247,70 @@ def test_full_size_sampled_rows(name):
         # row 0 of every head sees key 0 only: O = V[0] exactly, LSE = scale * q0.k0
         vv = synth.bf16_to_f32(v[:, :, 0, :]).astype(np.float64)
         assert np.array_equal(o[:, :, 0, :], vv)
+
+
+# --- sliding windows (bottom-right aligned) and causal with Nq != Nk ----------
+def _run_window(q, k, v, scale, window):
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    o, lse = fa.fwd(to_device(q), to_device(k), to_device(v), scale=scale, window=window)
+    torch.cuda.synchronize()
+    st, word = fa.fa_fwd_status(None, clear=True)
+    assert st == 0, f"kernel wait timed out, status word {word:#x}"
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def _assert_close_window(o, lse, o_ref, lse_ref, what):
+    # rows that see no key: LSE = -inf and O = 0 on both sides, exactly
+    empty = ~np.isfinite(lse_ref)
+    assert np.array_equal(~np.isfinite(lse), empty), f"{what}: empty-row pattern differs"
+    assert np.all(o[empty] == 0.0), f"{what}: O of an empty row is not 0"
+    full = ~empty
+    assert_close(o[full], lse[full], o_ref[full], lse_ref[full], what)
+
+
+WINDOWS = [(-1, 0), (0, 0), (64, 0), (200, 50), (127, 128), (-1, 300), (5, -1), (1000, 1000)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("window", WINDOWS)
+@pytest.mark.parametrize("nq,nk", [(700, 700), (300, 1000), (1000, 300), (257, 129)])
+def test_window_parity(nq, nk, window, d):
+    w = synth.Workload("win", 2, 2, nq, nk, d, False, seed=61 + nq + nk)
+    q, k, v = w.make()
+    o, lse = _run_window(q, k, v, w.scale, window)
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.scale, window=window)
+    _assert_close_window(o, lse, o_ref, lse_ref, f"window {window} {nq}x{nk} d{d}")
+
+
+def test_window_equal_to_causal_when_square():
+    w = synth.Workload("wc", 1, 3, 1000, 1000, 128, True, seed=62)
+    q, k, v = w.make()
+    o_w, l_w = _run_window(q, k, v, w.scale, (-1, 0))
+    o_c, l_c = run_gpu(q, k, v, w.scale, True, 1)
+    assert np.array_equal(o_w, o_c) and np.array_equal(l_w, l_c)
+
+
+def test_window_full_size_sampled_rows():
+    # long-context shape with a 1024-key causal window: most K/V tiles skipped
+    w = synth.WORKLOADS["long_8192_d128"]
+    q, k, v = w.make()
+    o, lse = _run_window(q, k, v, w.scale, (1024, 0))
+    rows = sample_rows(w.B, w.H, w.Nq, 300, seed=63)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, rows, w.scale, window=(1024, 0))
+    assert_close(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, "window 1024 at N=8192")
+
+
+def test_window_rejects_bad_bounds():
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    lse = torch.empty((1, 1, 128), dtype=torch.float32, device="cuda")
+    st = fa.fa_fwd_window(q.data_ptr(), q.data_ptr(), q.data_ptr(), o.data_ptr(), lse.data_ptr(), 1, 1, 128, 128, 64,
+                          0.125, -2, 0, None)
+    assert st == 3
