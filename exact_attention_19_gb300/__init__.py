@@ -15,7 +15,7 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "fa_fwd", "fa_fwd_window", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
+__all__ = ["FaError", "fa_fwd", "fa_fwd_window", "fa_fwd_splitkv", "fa_bwd", "fa_bwd_workspace_bytes", "bwd", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
            "fa_splitkv_heuristic", "NOALLOC_SCRATCH_BYTES",
            "fa_strerror", "fa_version", "fa_fwd_status", "fwd", "library_path", "load", "STATUS"]
 
@@ -72,6 +72,11 @@ def load():
         lib.fa_fwd_splitkv_noalloc.restype = i32
         lib.fa_fwd_window.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp]
         lib.fa_fwd_window.restype = i32
+        lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp,
+                               ctypes.c_size_t, vp]
+        lib.fa_bwd.restype = i32
+        lib.fa_bwd_workspace_bytes.argtypes = [i32, i32, i32]
+        lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         _lib = lib
     return _lib
 
@@ -123,6 +128,17 @@ def fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits) -> int:
 
 def fa_splitkv_heuristic(B, H, Nq, Nk, d, causal) -> int:
     return int(load().fa_splitkv_heuristic(int(B), int(H), int(Nq), int(Nk), int(d), int(causal)))
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, workspace, workspace_bytes,
+           stream) -> int:
+    """Raw C-ABI backward call; returns the status code (does not raise)."""
+    return int(load().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, int(B), int(H), int(Nq), int(Nk), int(d),
+                             float(scale), int(causal), workspace, int(workspace_bytes), stream))
+
+
+def fa_bwd_workspace_bytes(B, H, Nq) -> int:
+    return int(load().fa_bwd_workspace_bytes(int(B), int(H), int(Nq)))
 
 
 def fa_fwd_status(stream=None, clear: bool = False):
@@ -204,3 +220,38 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
     if st != 0:
         raise FaError(st)
     return out, lse
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+        workspace=None, stream=None):
+    """(dq, dk, dv) of attention by recomputation from the forward's ``lse``.
+
+    q, o, dout: [B, H, Nq, d]; k, v: [B, H, Nk, d], CUDA bf16, contiguous;
+    lse: fp32 [B, H, Nq] from ``fwd``.  ``workspace`` (CUDA tensor of at least
+    ``fa_bwd_workspace_bytes`` bytes) may be given to avoid allocating it.
+    """
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA torch.bfloat16 tensor")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if o.shape != q.shape or dout.shape != q.shape or v.shape != k.shape or k.shape[:2] != (B, H) or k.shape[3] != d:
+        raise ValueError("shape mismatch")
+    if lse.shape != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, Nq] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = fa_bwd_workspace_bytes(B, H, Nq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, scale, int(bool(causal)),
+                workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != 0:
+        raise FaError(st, "fa_bwd")
+    return dq, dk, dv

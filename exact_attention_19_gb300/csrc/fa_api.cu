@@ -11,6 +11,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_bwd_kernel.cuh"
 
 namespace {
 
@@ -53,6 +54,19 @@ cudaError_t set_smem_attr() {
 }
 
 template <int D>
+bool set_bwd_smem_attrs() {
+  using C = fa::BwdCfg<D>;
+  return cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(C::kSmemQ)) == cudaSuccess &&
+         cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(C::kSmemQ)) == cudaSuccess &&
+         cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(C::kSmemKV)) == cudaSuccess &&
+         cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(C::kSmemKV)) == cudaSuccess;
+}
+
+template <int D>
 bool set_smem_attrs() {
   return set_smem_attr<D, fa::kMaskNone, false>() == cudaSuccess &&
          set_smem_attr<D, fa::kMaskCausal, false>() == cudaSuccess &&
@@ -81,7 +95,8 @@ int prepare_device(int dev) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return FA_ERR_LAUNCH;
   g_dev_sms[dev] = sms;
-  if (!set_smem_attrs<64>() || !set_smem_attrs<128>()) return FA_ERR_LAUNCH;
+  if (!set_smem_attrs<64>() || !set_smem_attrs<128>() || !set_bwd_smem_attrs<64>() || !set_bwd_smem_attrs<128>())
+    return FA_ERR_LAUNCH;
   g_dev_state[dev].store(1, std::memory_order_release);
   return FA_OK;
 }
@@ -125,6 +140,18 @@ int launch_d(bool causal, const CUtensorMap& mq, const CUtensorMap& mk, const CU
              const fa::FwdParams& p, long long grid, cudaStream_t stream) {
   return causal ? launch<D, fa::kMaskCausal, SPLIT>(mq, mk, mv, p, grid, stream)
                 : launch<D, fa::kMaskNone, SPLIT>(mq, mk, mv, p, grid, stream);
+}
+
+template <int D, bool CAUSAL>
+int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
+               const fa::BwdParams& p, long long bh, cudaStream_t stream) {
+  using C = fa::BwdCfg<D>;
+  fa::fa_bwd_dq_kernel<D, CAUSAL><<<static_cast<unsigned>(bh * p.n_qt), C::kThreads, C::kSmemQ, stream>>>(
+      mq, mk, mv, mdo, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  fa::fa_bwd_dkdv_kernel<D, CAUSAL><<<static_cast<unsigned>(bh * p.n_kt), C::kThreads, C::kSmemKV, stream>>>(
+      mq, mk, mv, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 // Checks shared by fa_fwd and fa_fwd_splitkv.  On success fills the tensor
@@ -353,6 +380,66 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
   // empty slice writes weight 2^-inf), so nothing in the array has to be cleared.
   return fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, scratch,
                         FA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Backward pass
+// ---------------------------------------------------------------------------
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq) {
+  if (B <= 0 || H <= 0 || Nq <= 0) return 0;
+  const size_t nq_pad = (static_cast<size_t>(Nq) + 127) / 128 * 128;
+  return 2 * static_cast<size_t>(B) * H * nq_pad * sizeof(float);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+           void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal, void* workspace,
+           size_t workspace_bytes, cudaStream_t stream) {
+  const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, workspace};
+  for (const void* x : ptrs)
+    if (!x) return FA_ERR_NULL;
+  for (const void* x : ptrs)
+    if (reinterpret_cast<uintptr_t>(x) & 15u) return FA_ERR_ALIGN;
+  if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+  if (B <= 0 || H <= 0 || Nq <= 0 || Nk <= 0) return FA_ERR_SHAPE;
+  if (causal != 0 && causal != 1) return FA_ERR_SHAPE;
+  if (causal && Nq != Nk) return FA_ERR_CAUSAL_SHAPE;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long n_qt = (static_cast<long long>(Nq) + 127) / 128, n_kt = (static_cast<long long>(Nk) + 127) / 128;
+  if (static_cast<long long>(Nq > Nk ? Nq : Nk) * d * 2 >= (1ll << 40)) return FA_ERR_SHAPE;
+  if (BH >= (1ll << 31) || BH * n_qt >= (1ll << 31) || BH * n_kt >= (1ll << 31)) return FA_ERR_SHAPE;
+  if (workspace_bytes < fa_bwd_workspace_bytes(B, H, Nq)) return FA_ERR_WORKSPACE;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
+  const int prep = prepare_device(dev);
+  if (prep != FA_OK) return prep;
+  for (const void* x : ptrs)
+    if (!is_device_pointer(x, dev)) return FA_ERR_POINTER;
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_map(&mq, q, d, Nq, BH) || !make_map(&mk, k, d, Nk, BH) || !make_map(&mv, v, d, Nk, BH) ||
+      !make_map(&mdo, dout, d, Nq, BH))
+    return FA_ERR_LAUNCH;
+  fa::BwdParams p;
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.n_qt = static_cast<int>(n_qt);
+  p.n_kt = static_cast<int>(n_kt);
+  p.Nq_pad = static_cast<int>(n_qt * 128);
+  p.lse2 = static_cast<float*>(workspace);
+  p.dsum = p.lse2 + static_cast<size_t>(BH) * p.Nq_pad;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
+  if (d == 64)
+    return causal ? launch_bwd<64, true>(mq, mk, mv, mdo, p, BH, stream)
+                  : launch_bwd<64, false>(mq, mk, mv, mdo, p, BH, stream);
+  return causal ? launch_bwd<128, true>(mq, mk, mv, mdo, p, BH, stream)
+                : launch_bwd<128, false>(mq, mk, mv, mdo, p, BH, stream);
 }
 
 int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear) {

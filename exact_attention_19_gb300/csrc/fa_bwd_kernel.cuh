@@ -1,0 +1,618 @@
+// fa_bwd_kernel.cuh -- the attention backward pass for sm_103a, by
+// recomputation from the forward's LSE (page "llm-infra-atlas /
+// FlashAttention 01", section 5: P = exp(S * scale - LSE), dV = P^T dO,
+// dP = dO V^T, dS = P (dP - rowsum(dO O)), dQ = dS K * scale, dK = dS^T Q * scale).
+//
+// Two kernels, no atomics (the result is deterministic):
+//   fa_bwd_dq_kernel    one CTA per 128-row query tile: streams K_j, V_j and
+//                       accumulates dQ in TMEM; also writes, for the second
+//                       kernel, L = LSE * log2(e) and D = rowsum(dO * O) per
+//                       query, padded to whole query tiles (+inf and 0 past Nq).
+//   fa_bwd_dkdv_kernel  one CTA per 128-key tile, keys on TMEM lanes: streams
+//                       Q_i, dO_i (with their L and D) and accumulates dK, dV.
+// Both use the tcgen05 forms of the forward kernel: SS MMAs with K-major
+// operands for the two score-shaped products, TS MMAs (A = bf16 probabilities
+// or score gradients from TMEM, B = an MN-major tile from shared memory) for
+// the three accumulations.  Roles: warps 0-3 compute (one TMEM lane = one row
+// per thread), warp 4 TMA producer, warp 5 TMEM allocation and MMA issue.
+// Every wait is bounded as in the forward kernel.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "fa_ptx.cuh"
+
+namespace fa {
+
+struct BwdParams {
+  const void* o;      // bf16 [BH, Nq, D] forward output
+  const void* dout;   // bf16 [BH, Nq, D]
+  const float* lse;   // fp32 [BH, Nq] forward LSE (natural log)
+  void* dq;           // bf16 [BH, Nq, D]
+  void* dk;           // bf16 [BH, Nk, D]
+  void* dv;           // bf16 [BH, Nk, D]
+  float* lse2;        // workspace fp32 [BH, Nq_pad]: LSE * log2(e), +inf past Nq
+  float* dsum;        // workspace fp32 [BH, Nq_pad]: rowsum(dO * O), 0 past Nq
+  int Nq, Nk, Nq_pad;
+  int n_qt, n_kt;     // query / key tiles per head
+  float scale;        // softmax scale
+  float scale_log2;   // scale * log2(e)
+};
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kThreads = 192;
+  static constexpr int kBoxes = D / 64;
+  static constexpr uint32_t kBoxBytes = 128u * 128u;
+  static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D bf16
+  static constexpr int kRingQ = (D == 128) ? 5 : 8;           // dQ kernel: K/V ring slots
+  static constexpr int kRingKV = (D == 128) ? 4 : 8;          // dK/dV kernel: Q/dO ring slots
+  static constexpr uint32_t kSideBytes = 1024;                // L and D of one query tile
+  // dQ kernel smem: Q, dO, ring
+  static constexpr uint32_t kQRingOff = 2 * kTileBytes;
+  static constexpr uint32_t kQBarOff = kQRingOff + kRingQ * kTileBytes;
+  // dK/dV kernel smem: K, V, ring, side buffers
+  static constexpr uint32_t kKVRingOff = 2 * kTileBytes;
+  static constexpr uint32_t kKVSideOff = kKVRingOff + kRingKV * kTileBytes;
+  static constexpr uint32_t kKVBarOff = kKVSideOff + kRingKV * kSideBytes;
+  static constexpr uint32_t kBarBytes = 512;
+  static constexpr uint32_t kSmemQ = kQBarOff + kBarBytes + 1024;
+  static constexpr uint32_t kSmemKV = kKVBarOff + kBarBytes + 1024;
+  static constexpr uint32_t kIdescScore = idesc_bf16(128, 128, false);  // 128 x 128 over d
+  static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, true);       // 128 x D over 128 rows
+  static_assert(kSmemQ <= 232448 && kSmemKV <= 232448, "shared memory budget");
+};
+
+// ---------------------------------------------------------------------------
+// dQ kernel
+// ---------------------------------------------------------------------------
+// barriers: 0 q_full, 1 s_full, 2 dp_full, 3 s_free, 4 ds_full, 5 dq_full,
+// 6 drain, then ring full[kRingQ], empty[kRingQ]
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int R = C::kRingQ;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const sbase = smem_raw + (base - raw_addr);
+  const uint32_t bar0 = base + C::kQBarOff;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  auto full = [&](int s) -> uint32_t { return bar(7 + s); };
+  auto empty = [&](int s) -> uint32_t { return bar(7 + R + s); };
+  auto slot_addr = [&](int s) -> uint32_t { return base + C::kQRingOff + s * C::kTileBytes; };
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::kQBarOff + 448);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + C::kQBarOff + 452);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(0), 1);
+    mbar_init(bar(1), 1);
+    mbar_init(bar(2), 1);
+    mbar_init(bar(3), 128);
+    mbar_init(bar(4), 128);
+    mbar_init(bar(5), 1);
+    mbar_init(bar(6), 1);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // TMEM: S [0,128), dP [128,256) (dS overwrites its first 64 columns), dQ [256, 256 + D)
+  constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
+
+  const int bh = blockIdx.x / p.n_qt;
+  int qt = blockIdx.x % p.n_qt;
+  if (CAUSAL) qt = p.n_qt - 1 - qt;  // heaviest tile of each head first
+  const int row0 = qt * 128;
+  const int n_kv_all = (p.Nk + 127) / 128;
+  const int nkv = CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all;
+
+  if (warp == 4) {
+    // ======================= TMA producer =================================
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmDO);
+      mbar_arrive_expect_tx(bar(0), 2 * C::kTileBytes);
+      for (int b = 0; b < C::kBoxes; ++b) {
+        tma_load_3d(base + b * C::kBoxBytes, &tmQ, bar(0), b * 64, row0, bh);
+        tma_load_3d(base + C::kTileBytes + b * C::kBoxBytes, &tmDO, bar(0), b * 64, row0, bh);
+      }
+      int item = 0;
+      bool ok = true;
+      for (; item < 2 * nkv; ++item) {  // K_0, V_0, K_1, V_1, ...
+        const int s = item % R;
+        if (!(ok = mbar_wait(empty(s), ((item / R) & 1) ^ 1u, abort_flag))) break;
+        mbar_arrive_expect_tx(full(s), C::kTileBytes);
+        for (int b = 0; b < C::kBoxes; ++b)
+          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, (item & 1) ? &tmV : &tmK, full(s), b * 64, (item >> 1) * 128,
+                      bh);
+      }
+      if (!ok) report_wait_failure(abort_flag, 2u);
+      if (*abort_flag) {
+        for (int it = max(0, item - R); it < item; ++it) mbar_wait(full(it % R), (it / R) & 1, nullptr);
+        mbar_wait(bar(0), 0, nullptr);
+      }
+    }
+  } else if (warp == 5) {
+    // ======================= MMA issuer ====================================
+    if (lane == 0) {
+      const uint64_t dQd = sdesc_sw128(base, 16, 1024);                   // Q, K-major
+      const uint64_t dDOd = sdesc_sw128(base + C::kTileBytes, 16, 1024);  // dO, K-major
+      const uint64_t dRingK = sdesc_sw128(base + C::kQRingOff, 16, 1024);
+      const uint64_t dRingMN = sdesc_sw128(base + C::kQRingOff, C::kBoxBytes, 1024);
+      auto slot_off = [&](int s) -> uint64_t { return (s * C::kTileBytes) >> 4; };
+      // S = Q K_j^T or dP = dO V_j^T: 128 x 128 over d, both K-major
+      auto score = [&](uint64_t da, int s, uint32_t dst) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + dst, da + off, dRingK + slot_off(s) + off, C::kIdescScore, kk > 0 ? 1u : 0u);
+        }
+      };
+      // dQ += dS K_j: A = dS from TMEM (packed bf16 in the dP columns), B = K_j MN-major
+      auto acc_dq = [&](int s, bool acc_prev) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + kTmDQ, tmem + kTmDP + kk * 8, dRingMN + slot_off(s) + ((kk * 2048) >> 4), C::kIdescAcc,
+                 (acc_prev || kk > 0) ? 1u : 0u);
+      };
+      auto wait_item = [&](int it) -> bool { return mbar_wait(full(it % R), (it / R) & 1, abort_flag); };
+      bool ok = mbar_wait(bar(0), 0, abort_flag) && wait_item(0) && wait_item(1);
+      if (ok) {
+        tc_fence_after();
+        score(dQd, 0, kTmS);
+        mma_commit(bar(1));
+        score(dDOd, 1, kTmDP);
+        mma_commit(bar(2));
+        mma_commit(empty(1));  // V_0 is done
+      }
+      // Per K/V tile j: [S_j read, K_{j+1}, V_{j+1}] S_{j+1}; [dS_j] dQ += dS_j K_j; dP_{j+1}.
+      for (int j = 0; ok && j < nkv; ++j) {
+        const bool has_next = j + 1 < nkv;
+        const int sk = (2 * j) % R;
+        if (has_next) {
+          const int ik = 2 * j + 2, iv = 2 * j + 3;
+          const bool a = mbar_try_wait(bar(3), j & 1);
+          const bool b = mbar_try_wait(full(ik % R), (ik / R) & 1);
+          const bool c = mbar_try_wait(full(iv % R), (iv / R) & 1);
+          if (!(a && b && c)) {
+            if (!(ok = mbar_wait(bar(3), j & 1, abort_flag))) break;
+            if (!(ok = wait_item(ik))) break;
+            if (!(ok = wait_item(iv))) break;
+          }
+          tc_fence_after();
+          score(dQd, ik % R, kTmS);
+          mma_commit(bar(1));
+        }
+        if (!(ok = mbar_wait(bar(4), j & 1, abort_flag))) break;
+        tc_fence_after();
+        acc_dq(sk, j > 0);
+        mma_commit(empty(sk));  // K_j is done
+        if (j == nkv - 1) mma_commit(bar(5));
+        if (has_next) {
+          const int iv = 2 * j + 3;
+          score(dDOd, iv % R, kTmDP);
+          mma_commit(bar(2));
+          mma_commit(empty(iv % R));  // V_{j+1} is done
+        }
+      }
+      if (!ok) report_wait_failure(abort_flag, 4u);
+      mma_commit(bar(6));
+      mbar_wait(bar(6), 0, nullptr);
+    }
+  } else {
+    // ============== compute warpgroup (warps 0-3, one row per thread) =======
+    const int row_local = warp * 32 + lane;
+    const int row = row0 + row_local;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c = p.scale_log2;
+    const float NEG_INF = -__int_as_float(0x7f800000), POS_INF = __int_as_float(0x7f800000);
+    const bool valid = row < p.Nq;
+    const size_t grow = static_cast<size_t>(bh) * p.Nq + row;
+    // D = rowsum(dO * O) in fp32, L = LSE * log2(e); padding rows: P = 0
+    float dsum = 0.f, lse2 = POS_INF;
+    if (valid) {
+      const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + grow * D);
+      const uint4* drow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + grow * D);
+#pragma unroll 4
+      for (int i = 0; i < D / 8; ++i) {
+        const uint4 a = orow[i], b = drow[i];
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          dsum = fmaf(__uint_as_float(aw[t] << 16), __uint_as_float(bw[t] << 16), dsum);
+          dsum = fmaf(__uint_as_float(aw[t] & 0xFFFF0000u), __uint_as_float(bw[t] & 0xFFFF0000u), dsum);
+        }
+      }
+      lse2 = p.lse[grow] * 1.4426950408889634074f;
+    }
+    {
+      const size_t prow = static_cast<size_t>(bh) * p.Nq_pad + row;
+      p.lse2[prow] = lse2;
+      p.dsum[prow] = valid ? dsum : 0.f;
+    }
+    const float neg_lse2 = -lse2;
+    bool ok = true;
+    for (int j = 0; j < nkv; ++j) {
+      // ---- P = 2^(S*c - L) in registers, then S's columns are free
+      bool got = mbar_wait(bar(1), j & 1, abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32(lane_base + kTmS + 0, s0);
+      tmem_ld32(lane_base + kTmS + 32, s1);
+      tmem_ld32(lane_base + kTmS + 64, s2);
+      tmem_ld32(lane_base + kTmS + 96, s3);
+      tmem_ld_wait(s0);
+      reg_pin(s1);
+      reg_pin(s2);
+      reg_pin(s3);
+      tc_fence_before();
+      mbar_arrive(bar(3));
+      float* const f[4] = {reinterpret_cast<float*>(s0), reinterpret_cast<float*>(s1), reinterpret_cast<float*>(s2),
+                           reinterpret_cast<float*>(s3)};
+      // visible columns [0, lim): ragged key tail and the causal diagonal
+      int lim = p.Nk;
+      if (CAUSAL) lim = min(lim, row + 1);
+      lim -= j * 128;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float x0, x1;
+          fma2(x0, x1, f[q4][i], f[q4][i + 1], c, neg_lse2);
+          f[q4][i] = (q4 * 32 + i < lim) ? ex2(x0) : 0.f;
+          f[q4][i + 1] = (q4 * 32 + i + 1 < lim) ? ex2(x1) : 0.f;
+        }
+      // ---- dS = P (dP - D), bf16, into the first 64 columns of dP's region
+      got = mbar_wait(bar(2), j & 1, abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t dp[32];
+        tmem_ld32(lane_base + kTmDP + q4 * 32, dp);
+        tmem_ld_wait(dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = f[q4][2 * i] * (__uint_as_float(dp[2 * i]) - dsum);
+          const float b = f[q4][2 * i + 1] * (__uint_as_float(dp[2 * i + 1]) - dsum);
+          pk[i] = pack_bf16(a, b);
+        }
+        // columns [16*q4, 16*q4 + 16) were read by this or an earlier chunk
+        tmem_st16(lane_base + kTmDP + q4 * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(4));
+    }
+    if (!ok) report_wait_failure(abort_flag, 1u);
+    if (ok && nkv > 0) {
+      bool got = mbar_wait(bar(5), 0, abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        report_wait_failure(abort_flag, 8u);
+      } else {
+        tc_fence_after();
+        uint4* const out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kTmDQ + cc * 32, o);
+          tmem_ld_wait(o);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * p.scale, __uint_as_float(o[2 * i + 1]) * p.scale);
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) out[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dK / dV kernel
+// ---------------------------------------------------------------------------
+// barriers: 0 kv_full, 1 sd_full (S^T and dP^T), 2 p_full, 3 acc_full, 4 drain,
+// then ring full[kRingKV], empty[kRingKV]
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(192, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const BwdParams p) {
+  using C = BwdCfg<D>;
+  constexpr int R = C::kRingKV;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const sbase = smem_raw + (base - raw_addr);
+  const uint32_t bar0 = base + C::kKVBarOff;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  auto full = [&](int s) -> uint32_t { return bar(5 + s); };
+  auto empty = [&](int s) -> uint32_t { return bar(5 + R + s); };
+  auto slot_addr = [&](int s) -> uint32_t { return base + C::kKVRingOff + s * C::kTileBytes; };
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::kKVBarOff + 448);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + C::kKVBarOff + 452);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(0), 1);
+    mbar_init(bar(1), 1);
+    mbar_init(bar(2), 128);
+    mbar_init(bar(3), 1);
+    mbar_init(bar(4), 1);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_addr(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // TMEM: S^T [0,128) (P^T overwrites its first 64 columns), dP^T [128,256)
+  // (dS^T likewise), dV [256, 256 + D), dK [256 + D, 256 + 2D)
+  constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDV = 256, kTmDK = 256 + D;
+
+  const int bh = blockIdx.x / p.n_kt;
+  const int kt = blockIdx.x % p.n_kt;  // causal: small kt sees the most query tiles
+  const int key0 = kt * 128;
+  const int i0 = CAUSAL ? kt : 0;  // first query tile that sees this key tile
+  const int nq = p.n_qt - i0;      // query tiles to visit
+
+  if (warp == 4) {
+    // ======================= TMA producer =================================
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmDO);
+      mbar_arrive_expect_tx(bar(0), 2 * C::kTileBytes);
+      for (int b = 0; b < C::kBoxes; ++b) {
+        tma_load_3d(base + b * C::kBoxBytes, &tmK, bar(0), b * 64, key0, bh);
+        tma_load_3d(base + C::kTileBytes + b * C::kBoxBytes, &tmV, bar(0), b * 64, key0, bh);
+      }
+      int item = 0;
+      bool ok = true;
+      for (; item < 2 * nq; ++item) {  // Q_i (with its L, D), dO_i, ...
+        const int s = item % R;
+        const int i = i0 + (item >> 1);
+        if (!(ok = mbar_wait(empty(s), ((item / R) & 1) ^ 1u, abort_flag))) break;
+        if (item & 1) {
+          mbar_arrive_expect_tx(full(s), C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(slot_addr(s) + b * C::kBoxBytes, &tmDO, full(s), b * 64, i * 128, bh);
+        } else {
+          mbar_arrive_expect_tx(full(s), C::kTileBytes + C::kSideBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(slot_addr(s) + b * C::kBoxBytes, &tmQ, full(s), b * 64, i * 128, bh);
+          const size_t off = static_cast<size_t>(bh) * p.Nq_pad + static_cast<size_t>(i) * 128;
+          const uint32_t side = base + C::kKVSideOff + s * C::kSideBytes;
+          bulk_load(side, p.lse2 + off, 512, full(s));
+          bulk_load(side + 512, p.dsum + off, 512, full(s));
+        }
+      }
+      if (!ok) report_wait_failure(abort_flag, 2u);
+      if (*abort_flag) {
+        for (int it = max(0, item - R); it < item; ++it) mbar_wait(full(it % R), (it / R) & 1, nullptr);
+        mbar_wait(bar(0), 0, nullptr);
+      }
+    }
+  } else if (warp == 5) {
+    // ======================= MMA issuer ====================================
+    if (lane == 0) {
+      const uint64_t dKd = sdesc_sw128(base, 16, 1024);                  // K, K-major
+      const uint64_t dVd = sdesc_sw128(base + C::kTileBytes, 16, 1024);  // V, K-major
+      const uint64_t dRingK = sdesc_sw128(base + C::kKVRingOff, 16, 1024);
+      const uint64_t dRingMN = sdesc_sw128(base + C::kKVRingOff, C::kBoxBytes, 1024);
+      auto slot_off = [&](int s) -> uint64_t { return (s * C::kTileBytes) >> 4; };
+      // S^T = K Q_i^T or dP^T = V dO_i^T: 128 keys x 128 queries over d
+      auto score = [&](uint64_t da, int s, uint32_t dst) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss(tmem + dst, da + off, dRingK + slot_off(s) + off, C::kIdescScore, kk > 0 ? 1u : 0u);
+        }
+      };
+      // acc += A^T-tile (TMEM, 128 keys x 128 queries) times B_i (queries x D, MN-major)
+      auto accum = [&](uint32_t dst, uint32_t a_cols, int s, bool acc_prev) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + dst, tmem + a_cols + kk * 8, dRingMN + slot_off(s) + ((kk * 2048) >> 4), C::kIdescAcc,
+                 (acc_prev || kk > 0) ? 1u : 0u);
+      };
+      auto wait_item = [&](int it) -> bool { return mbar_wait(full(it % R), (it / R) & 1, abort_flag); };
+      bool ok = mbar_wait(bar(0), 0, abort_flag);
+      for (int ii = 0; ok && ii < nq; ++ii) {
+        const int iq = 2 * ii, ido = 2 * ii + 1;
+        const bool a = mbar_try_wait(full(iq % R), (iq / R) & 1);
+        const bool b = mbar_try_wait(full(ido % R), (ido / R) & 1);
+        if (!(a && b)) {
+          if (!(ok = wait_item(iq))) break;
+          if (!(ok = wait_item(ido))) break;
+        }
+        tc_fence_after();
+        score(dKd, iq % R, kTmS);
+        score(dVd, ido % R, kTmDP);
+        mma_commit(bar(1));
+        if (!(ok = mbar_wait(bar(2), ii & 1, abort_flag))) break;
+        tc_fence_after();
+        accum(kTmDV, kTmS, ido % R, ii > 0);  // dV += P^T dO_i
+        accum(kTmDK, kTmDP, iq % R, ii > 0);  // dK += dS^T Q_i
+        mma_commit(empty(iq % R));
+        mma_commit(empty(ido % R));
+      }
+      if (ok) mma_commit(bar(3));
+      if (!ok) report_wait_failure(abort_flag, 4u);
+      mma_commit(bar(4));
+      mbar_wait(bar(4), 0, nullptr);
+    }
+  } else {
+    // ============== compute warpgroup (warps 0-3, one key per thread) =======
+    const int key_local = warp * 32 + lane;
+    const int key = key0 + key_local;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int ii = 0; ii < nq; ++ii) {
+      const int i = i0 + ii;
+      const int s = (2 * ii) % R;  // slot of Q_i, which carries the side buffer
+      const float* const Ls = reinterpret_cast<const float*>(sbase + C::kKVSideOff + s * C::kSideBytes);
+      const float* const Ds = Ls + 128;
+      // the Q_i item's TMA barrier covers the side buffer (L, D) read below;
+      // S^T and dP^T come from the MMA commit
+      bool got = mbar_wait(full(s), ((2 * ii) / R) & 1, abort_flag) && mbar_wait(bar(1), ii & 1, abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t s0[32], s1[32], s2[32], s3[32];
+      tmem_ld32(lane_base + kTmS + 0, s0);
+      tmem_ld32(lane_base + kTmS + 32, s1);
+      tmem_ld32(lane_base + kTmS + 64, s2);
+      tmem_ld32(lane_base + kTmS + 96, s3);
+      tmem_ld_wait(s0);
+      reg_pin(s1);
+      reg_pin(s2);
+      reg_pin(s3);
+      float* const f[4] = {reinterpret_cast<float*>(s0), reinterpret_cast<float*>(s1), reinterpret_cast<float*>(s2),
+                           reinterpret_cast<float*>(s3)};
+      // causal: query q sees this key iff q >= key; only the diagonal tile masks
+      const int qlim = (CAUSAL && i == kt) ? key_local : 0;  // query columns < qlim are masked
+      // P^T = 2^(S^T c - L[q]); padding queries have L = +inf, so P^T = 0 there
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(Ls + q4 * 32 + i4 * 4);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            const int col = q4 * 32 + i4 * 4 + t;
+            const float x = fmaf(f[q4][i4 * 4 + t], c, -lv[t]);
+            f[q4][i4 * 4 + t] = (col >= qlim) ? ex2(x) : 0.f;
+          }
+        }
+#pragma unroll
+        for (int i2 = 0; i2 < 16; ++i2) pk[i2] = pack_bf16(f[q4][2 * i2], f[q4][2 * i2 + 1]);
+        tmem_st16(lane_base + kTmS + q4 * 16, pk);
+      }
+      // dS^T = P^T (dP^T - D[q]) into the first 64 columns of dP^T's region
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t dp[32];
+        tmem_ld32(lane_base + kTmDP + q4 * 32, dp);
+        tmem_ld_wait(dp);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(Ds + q4 * 32 + i4 * 4);
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+          for (int t = 0; t < 4; t += 2) {
+            const int e = i4 * 4 + t;
+            const float a = f[q4][e] * (__uint_as_float(dp[e]) - dv[t]);
+            const float b = f[q4][e + 1] * (__uint_as_float(dp[e + 1]) - dv[t + 1]);
+            pk[e / 2] = pack_bf16(a, b);
+          }
+        }
+        tmem_st16(lane_base + kTmDP + q4 * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(2));
+    }
+    if (!ok) report_wait_failure(abort_flag, 1u);
+    if (ok && nq > 0) {
+      bool got = mbar_wait(bar(3), 0, abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        report_wait_failure(abort_flag, 8u);
+      } else {
+        tc_fence_after();
+        const bool store = key < p.Nk;
+        const size_t grow = static_cast<size_t>(bh) * p.Nk + key;
+        uint4* const outv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dv) + grow * D);
+        uint4* const outk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dk) + grow * D);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + kTmDV + cc * 32, o);
+          tmem_ld_wait(o);
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pack_bf16(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+          if (store) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) outv[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+          tmem_ld32(lane_base + kTmDK + cc * 32, o);
+          tmem_ld_wait(o);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * p.scale, __uint_as_float(o[2 * i + 1]) * p.scale);
+          if (store) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) outk[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace fa

@@ -129,6 +129,30 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_spl
  * each of at least two K/V tiles) to fill them about once. */
 int fa_splitkv_heuristic(int B, int H, int Nq, int Nk, int d, int causal);
 
+/*
+ * fa_bwd -- attention backward pass by recomputation from the forward's LSE
+ * ("llm-infra-atlas / FlashAttention 01", section 5):
+ *   P = exp(scale * Q K^T - LSE),  dV = P^T dO,  dP = dO V^T,
+ *   D = rowsum(dO * O),  dS = P * (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q.
+ *
+ * q, o, dout, dq  [B, H, Nq, d] bf16;  k, v, dk, dv  [B, H, Nk, d] bf16;
+ * lse [B, H, Nq] fp32 as written by fa_fwd (natural log).  All contiguous,
+ * 16-byte aligned device memory of the current device; outputs must not
+ * overlap inputs.  causal as in fa_fwd (Nq == Nk).  Nq and Nk must be > 0.
+ * workspace: device memory of at least fa_bwd_workspace_bytes(B, H, Nq)
+ * bytes, owned by the caller (fp32 L = LSE * log2(e) and D per query, padded
+ * to whole 128-row tiles); not read before it is written.
+ * Two kernels run on `stream`: one per 128-row query tile for dQ (and L, D),
+ * then one per 128-key tile for dK and dV; no atomics, so the result does not
+ * depend on scheduling.  Errors as fa_fwd, plus FA_ERR_WORKSPACE.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes fa_bwd needs (0 for invalid sizes). */
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq);
+
 /* Size of the fixed device array fa_fwd_splitkv_noalloc works in. */
 #define FA_NOALLOC_SCRATCH_BYTES (16u << 20)
 

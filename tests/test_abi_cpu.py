@@ -116,3 +116,15 @@ def test_window_host_validation(lib):
     assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 64, 0.125, 0, -5, None) == 3
     assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 96, 0.125, 0, 0, None) == 4
     assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 0, 256, 64, 0.125, 10, 0, None) == 0
+
+
+def test_bwd_host_validation(lib):
+    args = [FAKE] * 9
+    assert fa.fa_bwd(*args, 1, 1, 128, 128, 64, 0.125, 0, FAKE, 1 << 20, None) != 1  # passes the NULL check
+    assert fa.fa_bwd(None, *args[1:], 1, 1, 128, 128, 64, 0.125, 0, FAKE, 1 << 20, None) == 1
+    assert fa.fa_bwd(*args, 1, 1, 128, 128, 64, 0.125, 0, None, 1 << 20, None) == 1
+    assert fa.fa_bwd(*args, 1, 1, 128, 128, 96, 0.125, 0, FAKE, 1 << 20, None) == 4
+    assert fa.fa_bwd(*args, 1, 1, 128, 256, 64, 0.125, 1, FAKE, 1 << 20, None) == 5
+    assert fa.fa_bwd(*args, 1, 1, 0, 128, 64, 0.125, 0, FAKE, 1 << 20, None) == 3
+    assert fa.fa_bwd(*args, 1, 1, 128, 128, 64, 0.125, 0, FAKE, 16, None) == 11
+    assert fa.fa_bwd_workspace_bytes(2, 3, 200) == 2 * 6 * 256 * 4

@@ -1,0 +1,126 @@
+"""Backward pass (fa_bwd) against the fp64 backward oracle (GB300 only).
+
+The GPU forward's own O and LSE feed the GPU backward (as a user would call
+it); the oracle recomputes everything in double precision from the same
+bf16 Q, K, V, dO.  Tolerance, per gradient tensor: max|d_gpu - d_ref| <=
+2e-2 * max|d_ref| (normwise: P and dS are rounded to bf16 before their
+MMAs and the gradients are returned in bf16, 2^-9 relative each; entry-wise
+relative bounds are meaningless for entries near zero).
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import backward
+from parity_util import to_device
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_attention_19_gb300 as fa
+    from exact_attention_19_gb300 import build
+
+    build.build()
+    fa.load()
+    backward.build()
+    yield
+
+
+def _gpu_grads(q, k, v, do, scale, causal):
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    tq, tk, tv, tdo = (to_device(x) for x in (q, k, v, do))
+    o, lse = fa.fwd(tq, tk, tv, causal=causal, scale=scale, n_splits=1)
+    dq, dk, dv = fa.bwd(tq, tk, tv, o, lse, tdo, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    st, word = fa.fa_fwd_status(None, clear=True)
+    assert st == 0, f"kernel wait timed out, status word {word:#x}"
+    return tuple(t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv))
+
+
+def _err(a, ref):
+    scale = np.max(np.abs(ref))
+    return float(np.max(np.abs(a - ref)) / scale) if scale > 0 else float(np.max(np.abs(a)))
+
+
+def _check(w: synth.Workload, what=""):
+    q, k, v = w.make()
+    do = synth.normal_bf16(w.seed + 7, 3, w.q_shape())
+    got = _gpu_grads(q, k, v, do, w.scale, w.causal)
+    ref = backward.attention_bwd(q, k, v, do, w.scale, w.causal)
+    errs = [_err(g, r) for g, r in zip(got, ref)]
+    for name, g, e in zip(("dq", "dk", "dv"), got, errs):
+        assert np.all(np.isfinite(g)), f"{what} {name} not finite"
+        assert e <= TOL, f"{what} {name} normwise error {e:.3e}"
+    return errs
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 63, 128, 129, 300, 1000])
+def test_bwd_square(n, d, causal):
+    _check(synth.Workload(f"bwd{n}", 1, 2, n, n, d, causal, seed=800 + n), f"n={n} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("nq,nk", [(100, 300), (513, 64), (256, 1000)])
+def test_bwd_rectangular(nq, nk, d):
+    _check(synth.Workload("bwd_rect", 2, 1, nq, nk, d, False, seed=810 + nq), f"{nq}x{nk} d={d}")
+
+
+def test_bwd_multi_head_and_wide_logits():
+    _check(synth.Workload("bwd_bh", 2, 3, 257, 257, 128, True, sigma_q=3.0, seed=820))
+    _check(synth.Workload("bwd_bh", 3, 2, 200, 200, 64, False, sigma_q=3.0, seed=821))
+
+
+def test_bwd_deterministic():
+    w = synth.Workload("bwd_det", 1, 3, 700, 700, 128, True, seed=830)
+    q, k, v = w.make()
+    do = synth.normal_bf16(831, 3, w.q_shape())
+    a = _gpu_grads(q, k, v, do, w.scale, True)
+    b = _gpu_grads(q, k, v, do, w.scale, True)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+
+
+def test_bwd_workspace_errors():
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    t = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device="cuda")
+    need = fa.fa_bwd_workspace_bytes(1, 1, 128)
+    assert need == 2 * 128 * 4
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = [t.data_ptr()] * 4 + [lse.data_ptr(), t.data_ptr()] + [torch.empty_like(t).data_ptr() for _ in range(3)]
+    assert fa.fa_bwd(*args, 1, 1, 128, 128, 64, 0.125, 0, ws.data_ptr(), need - 16, None) == 11
+    assert fa.fa_bwd(*args, 1, 1, 128, 128, 64, 0.125, 1, ws.data_ptr(), need, None) == 0
+    assert fa.fa_bwd(*args, 1, 1, 0, 128, 64, 0.125, 0, ws.data_ptr(), need, None) == 3
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_full_size_sampled(causal):
+    """B=4 H=32 N=8192 d=128: sampled dQ rows over all heads, sampled dK/dV keys of one head."""
+    from parity_util import sample_rows
+
+    w = synth.WORKLOADS["long_8192_d128_causal" if causal else "long_8192_d128"]
+    q, k, v = w.make()
+    do = synth.normal_bf16(w.seed + 7, 3, w.q_shape())
+    dq, dk, dv = _gpu_grads(q, k, v, do, w.scale, causal)
+    rows = sample_rows(w.B, w.H, w.Nq, 120, seed=840)
+    dq_ref = backward.attention_bwd_dq_rows(q, k, v, do, rows, w.scale, causal)
+    assert _err(dq.reshape(-1, w.d)[rows], dq_ref) <= TOL
+    bh = 37
+    keys = np.array([0, 1, 127, 128, 4000, 8190, 8191])
+    dk_ref, dv_ref = backward.attention_bwd_dkdv_keys(q, k, v, do, bh, keys, w.scale, causal)
+    assert _err(dk.reshape(-1, w.Nk, w.d)[bh][keys], dk_ref) <= TOL
+    assert _err(dv.reshape(-1, w.Nk, w.d)[bh][keys], dv_ref) <= TOL
