@@ -412,6 +412,56 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     return 0
 
 
+def run_bwd(args, w: synth.Workload, local_rank: int):
+    """Backward-pass timing line (not the headline metric): one fa_bwd per step."""
+    import torch
+
+    import exact_attention_19_gb300 as fa
+    from exact_attention_19_gb300 import build as fa_build
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fa_build.build()
+    q_h, k_h, v_h = w.make()
+    do_h = synth.normal_bf16(w.seed + 7, 3, w.q_shape())
+
+    def up(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v, do = up(q_h), up(k_h), up(v_h), up(do_h)
+    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale, n_splits=1)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
+               stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    st, word = fa.fa_fwd_status(None, clear=True)
+    if st != 0:
+        raise RuntimeError(f"kernel reported a wait timeout (status {word:#x})")
+    ms = e0.elapsed_time(e1) / args.steps
+    flops = 2.5 * w.flops
+    peaks, kind = load_peaks()
+    value = flops / (ms * 1e-3) / 1e12
+    print(json.dumps({"metric": "attention bwd TFLOP/s (2.5x forward FLOPs)", "value": value, "unit": UNIT,
+                      "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+                      "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
+                      "frac_of_peak": value / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                      "gpu_launches": 2 * args.steps}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,6 +472,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd: time fa_bwd instead (FLOPs counted as 2.5x the forward's)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -432,6 +484,8 @@ def main(argv=None):
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, w, rank)
+    if args.which == "bwd":
+        return run_bwd(args, w, local_rank)
     if world > 1:
         import torch.distributed as dist
 

@@ -186,4 +186,7 @@ WORKLOADS = {
     # stress: 16 heads, N = 32000, Q ~ N(0, 4^2), causal
     "stress_32000_d128_causal": Workload("stress_32000_d128_causal", 1, 16, 32000, 32000, 128, True,
                                          sigma_q=4.0, seed=1004),
+    # not one of the pages' shapes: the long-context shape at d = 64, to measure
+    # whether the exponential unit or the tensor pipe binds at the smaller head
+    "long_8192_d64": Workload("long_8192_d64", 4, 32, 8192, 8192, 64, False, seed=1005),
 }
