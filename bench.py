@@ -295,6 +295,10 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     if st != 0:
         raise RuntimeError(f"kernel reported a wait timeout during warm-up (status {word:#x})")
 
+    # denominator of the exponential-unit roofline, measured before the timed region
+    ex2_peak = fa.fa_probe_exp2(0, stream)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+
     try:
         props = torch.cuda.get_device_properties(dev)
         gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local_rank)
@@ -388,6 +392,16 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
                 "algorithmic_bytes": w.algorithmic_bytes,
                 "achieved_gbs": w.algorithmic_bytes / (ms_per_step * 1e-3) / 1e9}
 
+    # third roofline: exponentials (one ex2 per visible score) per SM clock
+    # against the probe's rate, at the median SM clock seen under load
+    ex2_per_step = w.B * w.H * w.Nq * w.Nk / (2 if w.causal else 1)
+    mufu = None
+    if clocks.get("sm_mhz"):
+        rate = ex2_per_step / (ms_per_step * 1e-3) / (float(clocks["sm_mhz"]) * 1e6) / n_sm
+        mufu = {"bound": "mufu", "achieved": rate, "peak": ex2_peak, "unit": "ex2/clk/SM", "frac": rate / ex2_peak,
+                "ex2_per_step": ex2_per_step, "sm_mhz": clocks["sm_mhz"], "sms": n_sm,
+                "peak_kind": "measured by fa_probe_exp2 (ex2.approx) on this GPU"}
+
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         q_np, k_np, v_np = q_h, k_h, v_h
@@ -401,7 +415,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(config_of(w, l2_note), n_splits=n_splits),
-        "roofline": roofline, "cpu_baseline": cpu,
+        "roofline": roofline, "mufu_roofline": mufu, "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(in_bytes),
                 "d2h_bytes_per_step": int(2 * o.numel() + 4 * lse.numel()), "ms_per_step": e2e_ms,
                 "steps": e2e_steps},

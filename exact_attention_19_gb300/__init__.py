@@ -60,6 +60,8 @@ def load():
         lib.fa_version.restype = i32
         lib.fa_fwd_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint), i32]
         lib.fa_fwd_status.restype = i32
+        lib.fa_probe_exp2.argtypes = [i32, ctypes.POINTER(ctypes.c_double), vp]
+        lib.fa_probe_exp2.restype = i32
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp,
                                        ctypes.c_size_t, vp]
         lib.fa_fwd_splitkv.restype = i32
@@ -146,6 +148,16 @@ def fa_fwd_status(stream=None, clear: bool = False):
     word = ctypes.c_uint(0)
     st = int(load().fa_fwd_status(stream, ctypes.byref(word), int(bool(clear))))
     return st, int(word.value)
+
+
+def fa_probe_exp2(method: int = 0, stream=None) -> float:
+    """2^x results per SM clock: method 0 ex2.approx (special-function unit), 1 cubic polynomial on the
+    FMA pipes.  Synchronises ``stream``."""
+    rate = ctypes.c_double(0.0)
+    st = int(load().fa_probe_exp2(int(method), ctypes.byref(rate), stream))
+    if st != 0:
+        raise FaError(st, "fa_probe_exp2")
+    return float(rate.value)
 
 
 def _stream_handle(stream):

@@ -1,7 +1,8 @@
 """Build libfa_gb300.so in-tree with nvcc (sm_103a only).
 
-The library is a single translation unit: the C-ABI front end and the four
-kernel instantiations (d in {64, 128} x causal in {0, 1}).
+Two translation units: fa_api.cu (the C-ABI front end with every forward,
+split-KV merge and backward kernel instantiation) and fa_probe.cu (the
+exp2-throughput probe), compiled in one nvcc call.
 """
 from __future__ import annotations
 
@@ -16,8 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libfa_gb300.so")
-SOURCES = [os.path.join(CSRC, "fa_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_ptx.cuh", "fa_fwd_kernel.cuh")] + [
+SOURCES = [os.path.join(CSRC, "fa_api.cu"), os.path.join(CSRC, "fa_probe.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_ptx.cuh", "fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh")] + [
     os.path.join(INCLUDE, "fa.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -198,6 +198,24 @@ int fa_version(void);
  */
 int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear);
 
+/*
+ * fa_probe_exp2 -- measure how many 2^x results per SM clock cycle the current
+ * device produces (median over the SMs of one CTA per SM running independent
+ * exp2 chains).  Not an operation of the pages: method 0 times ex2.approx on
+ * the special-function unit, the denominator of the forward kernel's
+ * exponential-unit roofline; method 1 times a cubic polynomial on the FMA and
+ * integer pipes, the kind of offload that the page "pinghaoyang FlashAttention
+ * 1-4 guide" (FA4 section, emulated exponential) describes for Blackwell.
+ *
+ * method      0 or 1 (anything else: FA_ERR_SHAPE).
+ * per_clk_sm  host pointer receiving the rate.
+ * stream      the probe runs on it; the call synchronises the stream.
+ * Uses no caller memory.  Returns FA_ERR_NULL, FA_ERR_SHAPE, FA_ERR_DEVICE
+ * (not compute capability 10.3) or FA_ERR_LAUNCH; the value is written only
+ * on FA_OK.
+ */
+int fa_probe_exp2(int method, double* per_clk_sm, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -49,6 +49,13 @@ def test_version_and_strerror(lib):
     assert fa.fa_strerror(12345) == "unknown status"
 
 
+def test_probe_rejects_bad_arguments(lib):
+    import ctypes
+
+    assert lib.fa_probe_exp2(0, None, None) == 1  # FA_ERR_NULL, before any device call
+    assert lib.fa_probe_exp2(2, ctypes.byref(ctypes.c_double()), None) == 3  # FA_ERR_SHAPE
+
+
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
 
 
