@@ -13,9 +13,16 @@
 // Both use the tcgen05 forms of the forward kernel: SS MMAs with K-major
 // operands for the two score-shaped products, TS MMAs (A = bf16 probabilities
 // or score gradients from TMEM, B = an MN-major tile from shared memory) for
-// the three accumulations.  Roles: warps 0-3 compute (one TMEM lane = one row
-// per thread), warp 4 TMA producer, warp 5 TMEM allocation and MMA issue.
-// Every wait is bounded as in the forward kernel.
+// the three accumulations.  Roles: warps 0-7 compute, warp 8 TMA producer,
+// warp 9 TMEM allocation and MMA issue.  Compute warp 4h + q holds TMEM lanes
+// 32q..32q+31 (one row per thread) and column half h of every 128-column
+// tile: the elementwise work (P from the stored L, dS from the stored D) needs
+// no reduction along a row, so the two halves never communicate, and two
+// warps per SM sub-partition keep twice the exponentials in flight.  Each half
+// writes its bf16 results into its own columns (64h..64h+31), so no half
+// overwrites values the other has yet to read; the MMAs take their A operand
+// from columns 64 (kk / 4) + 8 (kk % 4).  Every wait is bounded as in the
+// forward kernel.
 #pragma once
 
 #include <cstdint>
@@ -43,7 +50,7 @@ struct BwdParams {
 template <int D>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 320;
   static constexpr int kBoxes = D / 64;
   static constexpr uint32_t kBoxBytes = 128u * 128u;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;  // 128 rows x D bf16
@@ -71,7 +78,7 @@ struct BwdCfg {
 // barriers: 0 q_full, 1 s_full, 2 dp_full, 3 s_free, 4 ds_full, 5 dq_full,
 // 6 drain, then ring full[kRingQ], empty[kRingQ]
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const BwdParams p) {
@@ -94,8 +101,8 @@ __global__ void __launch_bounds__(192, 1)
     mbar_init(bar(0), 1);
     mbar_init(bar(1), 1);
     mbar_init(bar(2), 1);
-    mbar_init(bar(3), 128);
-    mbar_init(bar(4), 128);
+    mbar_init(bar(3), 256);
+    mbar_init(bar(4), 256);
     mbar_init(bar(5), 1);
     mbar_init(bar(6), 1);
     for (int s = 0; s < R; ++s) {
@@ -105,7 +112,7 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -113,8 +120,10 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // TMEM: S [0,128), dP [128,256) (dS overwrites its first 64 columns), dQ [256, 256 + D)
-  constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 256;
+  // TMEM: S [0,128), two dP buffers [128,256) and [256,384) (K/V tile j uses
+  // buffer j % 2; dS_j overwrites part of it), dQ [384, 384 + D)
+  constexpr uint32_t kTmS = 0, kTmDP = 128, kTmDQ = 384;
+  static_assert(kTmDQ + D <= 512, "TMEM columns");
 
   const int bh = blockIdx.x / p.n_qt;
   int qt = blockIdx.x % p.n_qt;
@@ -123,7 +132,7 @@ __global__ void __launch_bounds__(192, 1)
   const int n_kv_all = (p.Nk + 127) / 128;
   const int nkv = CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ======================= TMA producer =================================
     if (lane == 0) {
       tma_prefetch_map(&tmQ);
@@ -137,12 +146,14 @@ __global__ void __launch_bounds__(192, 1)
       }
       int item = 0;
       bool ok = true;
-      for (; item < 2 * nkv; ++item) {  // K_0, V_0, K_1, V_1, ...
+      // V_0, K_0, V_1, K_1, ...: V_j is done early (after dP_j), K_j late (after
+      // dQ_j), so each V reuses the slot of a K released two tiles before
+      for (; item < 2 * nkv; ++item) {
         const int s = item % R;
         if (!(ok = mbar_wait(empty(s), ((item / R) & 1) ^ 1u, abort_flag))) break;
         mbar_arrive_expect_tx(full(s), C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, (item & 1) ? &tmV : &tmK, full(s), b * 64, (item >> 1) * 128,
+          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, (item & 1) ? &tmK : &tmV, full(s), b * 64, (item >> 1) * 128,
                       bh);
       }
       if (!ok) report_wait_failure(abort_flag, 2u);
@@ -151,7 +162,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait(bar(0), 0, nullptr);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ======================= MMA issuer ====================================
     if (lane == 0) {
       const uint64_t dQd = sdesc_sw128(base, 16, 1024);                   // Q, K-major
@@ -167,29 +178,35 @@ __global__ void __launch_bounds__(192, 1)
           mma_ss(tmem + dst, da + off, dRingK + slot_off(s) + off, C::kIdescScore, kk > 0 ? 1u : 0u);
         }
       };
-      // dQ += dS K_j: A = dS from TMEM (packed bf16 in the dP columns), B = K_j MN-major
-      auto acc_dq = [&](int s, bool acc_prev) {
+      // dQ += dS_j K_j: A = dS_j from TMEM (packed bf16 in dP buffer j % 2, keys
+      // 16kk.. at column 64 (kk / 4) + 8 (kk % 4)), B = K_j MN-major
+      auto acc_dq = [&](int s, uint32_t dp_buf, bool acc_prev) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + kTmDQ, tmem + kTmDP + kk * 8, dRingMN + slot_off(s) + ((kk * 2048) >> 4), C::kIdescAcc,
-                 (acc_prev || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kTmDQ, tmem + dp_buf + (kk >> 2) * 64 + (kk & 3) * 8,
+                 dRingMN + slot_off(s) + ((kk * 2048) >> 4), C::kIdescAcc, (acc_prev || kk > 0) ? 1u : 0u);
       };
       auto wait_item = [&](int it) -> bool { return mbar_wait(full(it % R), (it / R) & 1, abort_flag); };
+      // ring items: V_j = 2j, K_j = 2j + 1
       bool ok = mbar_wait(bar(0), 0, abort_flag) && wait_item(0) && wait_item(1);
       if (ok) {
         tc_fence_after();
-        score(dQd, 0, kTmS);
+        score(dQd, 1, kTmS);
         mma_commit(bar(1));
-        score(dDOd, 1, kTmDP);
+        score(dDOd, 0, kTmDP);
         mma_commit(bar(2));
-        mma_commit(empty(1));  // V_0 is done
+        mma_commit(empty(0));  // V_0 is done
       }
-      // Per K/V tile j: [S_j read, K_{j+1}, V_{j+1}] S_{j+1}; [dS_j] dQ += dS_j K_j; dP_{j+1}.
+      // Per K/V tile j: [S_j read, K_{j+1}, V_{j+1}] S_{j+1}, dP_{j+1}; [dS_j] dQ += dS_j K_j.
+      // The next tile's two score products run while the warps turn P_j and
+      // dP_j into dS_j: S_{j+1} may overwrite S once it has been read (P stays
+      // in registers), and dP_{j+1} goes to the other dP buffer, whose last
+      // reader (dQ += dS_{j-1} K_{j-1}) was issued before it.
       for (int j = 0; ok && j < nkv; ++j) {
         const bool has_next = j + 1 < nkv;
-        const int sk = (2 * j) % R;
+        const int sk = (2 * j + 1) % R;
         if (has_next) {
-          const int ik = 2 * j + 2, iv = 2 * j + 3;
+          const int iv = 2 * j + 2, ik = 2 * j + 3;
           const bool a = mbar_try_wait(bar(3), j & 1);
           const bool b = mbar_try_wait(full(ik % R), (ik / R) & 1);
           const bool c = mbar_try_wait(full(iv % R), (iv / R) & 1);
@@ -201,33 +218,33 @@ __global__ void __launch_bounds__(192, 1)
           tc_fence_after();
           score(dQd, ik % R, kTmS);
           mma_commit(bar(1));
-        }
-        if (!(ok = mbar_wait(bar(4), j & 1, abort_flag))) break;
-        tc_fence_after();
-        acc_dq(sk, j > 0);
-        mma_commit(empty(sk));  // K_j is done
-        if (j == nkv - 1) mma_commit(bar(5));
-        if (has_next) {
-          const int iv = 2 * j + 3;
-          score(dDOd, iv % R, kTmDP);
+          score(dDOd, iv % R, kTmDP + ((j + 1) & 1) * 128);
           mma_commit(bar(2));
           mma_commit(empty(iv % R));  // V_{j+1} is done
         }
+        if (!(ok = mbar_wait(bar(4), j & 1, abort_flag))) break;
+        tc_fence_after();
+        acc_dq(sk, kTmDP + (j & 1) * 128, j > 0);
+        mma_commit(empty(sk));  // K_j is done
+        if (j == nkv - 1) mma_commit(bar(5));
       }
       if (!ok) report_wait_failure(abort_flag, 4u);
       mma_commit(bar(6));
       mbar_wait(bar(6), 0, nullptr);
     }
   } else {
-    // ============== compute warpgroup (warps 0-3, one row per thread) =======
-    const int row_local = warp * 32 + lane;
+    // ============== compute warps (0-7: one row per thread, one column half) =====
+    const int h = warp >> 2;  // keys 64h..64h+63 of each K/V tile, dQ columns h*D/2..
+    const int wq = warp & 3;  // TMEM lane quarter
+    const int row_local = wq * 32 + lane;
     const int row = row0 + row_local;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float c = p.scale_log2;
     const float NEG_INF = -__int_as_float(0x7f800000), POS_INF = __int_as_float(0x7f800000);
     const bool valid = row < p.Nq;
     const size_t grow = static_cast<size_t>(bh) * p.Nq + row;
-    // D = rowsum(dO * O) in fp32, L = LSE * log2(e); padding rows: P = 0
+    // D = rowsum(dO * O) in fp32, L = LSE * log2(e); padding rows: P = 0.
+    // Both halves compute the whole row's D, in the same order (same value).
     float dsum = 0.f, lse2 = POS_INF;
     if (valid) {
       const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + grow * D);
@@ -244,12 +261,15 @@ __global__ void __launch_bounds__(192, 1)
       }
       lse2 = p.lse[grow] * 1.4426950408889634074f;
     }
-    {
+    if (h == 0) {
       const size_t prow = static_cast<size_t>(bh) * p.Nq_pad + row;
       p.lse2[prow] = lse2;
       p.dsum[prow] = valid ? dsum : 0.f;
     }
     const float neg_lse2 = -lse2;
+    const uint32_t tSh = lane_base + kTmS + h * 64;    // this half's S columns
+    // this half's columns of dP buffer 0 (tile j uses buffer j % 2; dS lands in the first 32)
+    const uint32_t tDPh = lane_base + kTmDP + h * 64;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
       // ---- P = 2^(S*c - L) in registers, then S's columns are free
@@ -260,33 +280,28 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      uint32_t s0[32], s1[32], s2[32], s3[32];
-      tmem_ld32(lane_base + kTmS + 0, s0);
-      tmem_ld32(lane_base + kTmS + 32, s1);
-      tmem_ld32(lane_base + kTmS + 64, s2);
-      tmem_ld32(lane_base + kTmS + 96, s3);
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tSh + 0, s0);
+      tmem_ld32(tSh + 32, s1);
       tmem_ld_wait(s0);
       reg_pin(s1);
-      reg_pin(s2);
-      reg_pin(s3);
       tc_fence_before();
       mbar_arrive(bar(3));
-      float* const f[4] = {reinterpret_cast<float*>(s0), reinterpret_cast<float*>(s1), reinterpret_cast<float*>(s2),
-                           reinterpret_cast<float*>(s3)};
-      // visible columns [0, lim): ragged key tail and the causal diagonal
+      float* const f[2] = {reinterpret_cast<float*>(s0), reinterpret_cast<float*>(s1)};
+      // visible columns of this half [0, lim): ragged key tail and the causal diagonal
       int lim = p.Nk;
       if (CAUSAL) lim = min(lim, row + 1);
-      lim -= j * 128;
+      lim -= j * 128 + h * 64;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4)
+      for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float x0, x1;
-          fma2(x0, x1, f[q4][i], f[q4][i + 1], c, neg_lse2);
-          f[q4][i] = (q4 * 32 + i < lim) ? ex2(x0) : 0.f;
-          f[q4][i + 1] = (q4 * 32 + i + 1 < lim) ? ex2(x1) : 0.f;
+          fma2(x0, x1, f[q2][i], f[q2][i + 1], c, neg_lse2);
+          f[q2][i] = (q2 * 32 + i < lim) ? ex2(x0) : 0.f;
+          f[q2][i + 1] = (q2 * 32 + i + 1 < lim) ? ex2(x1) : 0.f;
         }
-      // ---- dS = P (dP - D), bf16, into the first 64 columns of dP's region
+      // ---- dS = P (dP - D), bf16, into the first 32 columns of this half's dP
       got = mbar_wait(bar(2), j & 1, abort_flag);
       got = __all_sync(0xffffffffu, got);
       if (!got) {
@@ -295,19 +310,20 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t dp[32];
-        tmem_ld32(lane_base + kTmDP + q4 * 32, dp);
+        const uint32_t tdp = tDPh + (j & 1) * 128;
+        tmem_ld32(tdp + q2 * 32, dp);
         tmem_ld_wait(dp);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = f[q4][2 * i] * (__uint_as_float(dp[2 * i]) - dsum);
-          const float b = f[q4][2 * i + 1] * (__uint_as_float(dp[2 * i + 1]) - dsum);
+          const float a = f[q2][2 * i] * (__uint_as_float(dp[2 * i]) - dsum);
+          const float b = f[q2][2 * i + 1] * (__uint_as_float(dp[2 * i + 1]) - dsum);
           pk[i] = pack_bf16(a, b);
         }
-        // columns [16*q4, 16*q4 + 16) were read by this or an earlier chunk
-        tmem_st16(lane_base + kTmDP + q4 * 16, pk);
+        // columns [16*q2, 16*q2 + 16) of this half were read by the first chunk
+        tmem_st16(tdp + q2 * 16, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -321,11 +337,11 @@ __global__ void __launch_bounds__(192, 1)
         report_wait_failure(abort_flag, 8u);
       } else {
         tc_fence_after();
-        uint4* const out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * D);
+        uint4* const out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * D + h * (D / 2));
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 64; ++cc) {
           uint32_t o[32];
-          tmem_ld32(lane_base + kTmDQ + cc * 32, o);
+          tmem_ld32(lane_base + kTmDQ + h * (D / 2) + cc * 32, o);
           tmem_ld_wait(o);
           uint32_t w[16];
 #pragma unroll
@@ -341,7 +357,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -351,10 +367,11 @@ __global__ void __launch_bounds__(192, 1)
 // ---------------------------------------------------------------------------
 // dK / dV kernel
 // ---------------------------------------------------------------------------
-// barriers: 0 kv_full, 1 sd_full (S^T and dP^T), 2 p_full, 3 acc_full, 4 drain,
-// then ring full[kRingKV], empty[kRingKV]
+// barriers: 0 kv_full, 1 s_full (S^T), 2 p_done (P^T written), 3 acc_full,
+// 4 drain, 5 dp_full (dP^T), 6 ds_done (dS^T written), then ring
+// full[kRingKV], empty[kRingKV]
 template <int D, bool CAUSAL>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const BwdParams p) {
@@ -366,8 +383,8 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* const sbase = smem_raw + (base - raw_addr);
   const uint32_t bar0 = base + C::kKVBarOff;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  auto full = [&](int s) -> uint32_t { return bar(5 + s); };
-  auto empty = [&](int s) -> uint32_t { return bar(5 + R + s); };
+  auto full = [&](int s) -> uint32_t { return bar(7 + s); };
+  auto empty = [&](int s) -> uint32_t { return bar(7 + R + s); };
   auto slot_addr = [&](int s) -> uint32_t { return base + C::kKVRingOff + s * C::kTileBytes; };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::kKVBarOff + 448);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + C::kKVBarOff + 452);
@@ -376,9 +393,11 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     mbar_init(bar(0), 1);
     mbar_init(bar(1), 1);
-    mbar_init(bar(2), 128);
+    mbar_init(bar(2), 256);
     mbar_init(bar(3), 1);
     mbar_init(bar(4), 1);
+    mbar_init(bar(5), 1);
+    mbar_init(bar(6), 256);
     for (int s = 0; s < R; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
@@ -386,7 +405,7 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_addr(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -404,7 +423,7 @@ __global__ void __launch_bounds__(192, 1)
   const int i0 = CAUSAL ? kt : 0;  // first query tile that sees this key tile
   const int nq = p.n_qt - i0;      // query tiles to visit
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ======================= TMA producer =================================
     if (lane == 0) {
       tma_prefetch_map(&tmQ);
@@ -442,7 +461,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_wait(bar(0), 0, nullptr);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ======================= MMA issuer ====================================
     if (lane == 0) {
       const uint64_t dKd = sdesc_sw128(base, 16, 1024);                  // K, K-major
@@ -458,33 +477,62 @@ __global__ void __launch_bounds__(192, 1)
           mma_ss(tmem + dst, da + off, dRingK + slot_off(s) + off, C::kIdescScore, kk > 0 ? 1u : 0u);
         }
       };
-      // acc += A^T-tile (TMEM, 128 keys x 128 queries) times B_i (queries x D, MN-major)
+      // acc += A^T-tile (TMEM, 128 keys x 128 queries; queries 16kk.. at column
+      // a_cols + 64 (kk / 4) + 8 (kk % 4)) times B_i (queries x D, MN-major)
       auto accum = [&](uint32_t dst, uint32_t a_cols, int s, bool acc_prev) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + dst, tmem + a_cols + kk * 8, dRingMN + slot_off(s) + ((kk * 2048) >> 4), C::kIdescAcc,
-                 (acc_prev || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + dst, tmem + a_cols + (kk >> 2) * 64 + (kk & 3) * 8, dRingMN + slot_off(s) + ((kk * 2048) >> 4),
+                 C::kIdescAcc, (acc_prev || kk > 0) ? 1u : 0u);
       };
       auto wait_item = [&](int it) -> bool { return mbar_wait(full(it % R), (it / R) & 1, abort_flag); };
-      bool ok = mbar_wait(bar(0), 0, abort_flag);
+      bool ok = mbar_wait(bar(0), 0, abort_flag) && wait_item(0) && wait_item(1);
+      if (ok) {
+        tc_fence_after();
+        score(dKd, 0, kTmS);
+        mma_commit(bar(1));
+        score(dVd, 1, kTmDP);
+        mma_commit(bar(5));
+      }
+      // Per query tile i: [P^T_i written, Q_{i+1}] dV += P^T_i dO_i, S^T_{i+1};
+      // [dS^T_i written, dO_{i+1}] dK += dS^T_i Q_i, dP^T_{i+1}.  The next tile's
+      // S^T runs while the warps turn dP^T_i into dS^T_i, and its dP^T while they
+      // exponentiate S^T_{i+1}: S^T_{i+1} overwrites P^T_i only after the dV
+      // product that reads it (issued first), dP^T_{i+1} overwrites dS^T_i only
+      // after the dK product.
       for (int ii = 0; ok && ii < nq; ++ii) {
         const int iq = 2 * ii, ido = 2 * ii + 1;
-        const bool a = mbar_try_wait(full(iq % R), (iq / R) & 1);
-        const bool b = mbar_try_wait(full(ido % R), (ido / R) & 1);
-        if (!(a && b)) {
-          if (!(ok = wait_item(iq))) break;
-          if (!(ok = wait_item(ido))) break;
+        const bool has_next = ii + 1 < nq;
+        {
+          const bool a = mbar_try_wait(bar(2), ii & 1);
+          const bool b = !has_next || mbar_try_wait(full((iq + 2) % R), ((iq + 2) / R) & 1);
+          if (!(a && b)) {
+            if (!(ok = mbar_wait(bar(2), ii & 1, abort_flag))) break;
+            if (has_next && !(ok = wait_item(iq + 2))) break;
+          }
         }
         tc_fence_after();
-        score(dKd, iq % R, kTmS);
-        score(dVd, ido % R, kTmDP);
-        mma_commit(bar(1));
-        if (!(ok = mbar_wait(bar(2), ii & 1, abort_flag))) break;
-        tc_fence_after();
         accum(kTmDV, kTmS, ido % R, ii > 0);  // dV += P^T dO_i
+        mma_commit(empty(ido % R));           // dO_i is done
+        if (has_next) {
+          score(dKd, (iq + 2) % R, kTmS);  // S^T_{i+1}
+          mma_commit(bar(1));
+        }
+        {
+          const bool a = mbar_try_wait(bar(6), ii & 1);
+          const bool b = !has_next || mbar_try_wait(full((ido + 2) % R), ((ido + 2) / R) & 1);
+          if (!(a && b)) {
+            if (!(ok = mbar_wait(bar(6), ii & 1, abort_flag))) break;
+            if (has_next && !(ok = wait_item(ido + 2))) break;
+          }
+        }
+        tc_fence_after();
         accum(kTmDK, kTmDP, iq % R, ii > 0);  // dK += dS^T Q_i
-        mma_commit(empty(iq % R));
-        mma_commit(empty(ido % R));
+        mma_commit(empty(iq % R));            // Q_i (and its L, D) is done
+        if (has_next) {
+          score(dVd, (ido + 2) % R, kTmDP);  // dP^T_{i+1}
+          mma_commit(bar(5));
+        }
       }
       if (ok) mma_commit(bar(3));
       if (!ok) report_wait_failure(abort_flag, 4u);
@@ -492,19 +540,23 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(bar(4), 0, nullptr);
     }
   } else {
-    // ============== compute warpgroup (warps 0-3, one key per thread) =======
-    const int key_local = warp * 32 + lane;
+    // ============== compute warps (0-7: one key per thread, one column half) =====
+    const int h = warp >> 2;  // queries 64h..64h+63 of each query tile, dK/dV columns h*D/2..
+    const int wq = warp & 3;  // TMEM lane quarter
+    const int key_local = wq * 32 + lane;
     const int key = key0 + key_local;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t tSh = lane_base + kTmS + h * 64;    // this half's S^T columns (P^T lands in the first 32)
+    const uint32_t tDPh = lane_base + kTmDP + h * 64;  // this half's dP^T columns (dS^T likewise)
     const float c = p.scale_log2;
     bool ok = true;
     for (int ii = 0; ii < nq; ++ii) {
       const int i = i0 + ii;
       const int s = (2 * ii) % R;  // slot of Q_i, which carries the side buffer
-      const float* const Ls = reinterpret_cast<const float*>(sbase + C::kKVSideOff + s * C::kSideBytes);
+      const float* const Ls = reinterpret_cast<const float*>(sbase + C::kKVSideOff + s * C::kSideBytes) + h * 64;
       const float* const Ds = Ls + 128;
       // the Q_i item's TMA barrier covers the side buffer (L, D) read below;
-      // S^T and dP^T come from the MMA commit
+      // S^T_i comes from its MMA commit (dP^T_i, from its own, is waited for later)
       bool got = mbar_wait(full(s), ((2 * ii) / R) & 1, abort_flag) && mbar_wait(bar(1), ii & 1, abort_flag);
       got = __all_sync(0xffffffffu, got);
       if (!got) {
@@ -512,62 +564,66 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      uint32_t s0[32], s1[32], s2[32], s3[32];
-      tmem_ld32(lane_base + kTmS + 0, s0);
-      tmem_ld32(lane_base + kTmS + 32, s1);
-      tmem_ld32(lane_base + kTmS + 64, s2);
-      tmem_ld32(lane_base + kTmS + 96, s3);
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tSh + 0, s0);
+      tmem_ld32(tSh + 32, s1);
       tmem_ld_wait(s0);
       reg_pin(s1);
-      reg_pin(s2);
-      reg_pin(s3);
-      float* const f[4] = {reinterpret_cast<float*>(s0), reinterpret_cast<float*>(s1), reinterpret_cast<float*>(s2),
-                           reinterpret_cast<float*>(s3)};
+      float* const f[2] = {reinterpret_cast<float*>(s0), reinterpret_cast<float*>(s1)};
       // causal: query q sees this key iff q >= key; only the diagonal tile masks
-      const int qlim = (CAUSAL && i == kt) ? key_local : 0;  // query columns < qlim are masked
+      const int qlim = (CAUSAL && i == kt) ? key_local - h * 64 : 0;  // this half's columns < qlim are masked
       // P^T = 2^(S^T c - L[q]); padding queries have L = +inf, so P^T = 0 there
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t pk[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(Ls + q4 * 32 + i4 * 4);
+          const float4 l4 = *reinterpret_cast<const float4*>(Ls + q2 * 32 + i4 * 4);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
           for (int t = 0; t < 4; ++t) {
-            const int col = q4 * 32 + i4 * 4 + t;
-            const float x = fmaf(f[q4][i4 * 4 + t], c, -lv[t]);
-            f[q4][i4 * 4 + t] = (col >= qlim) ? ex2(x) : 0.f;
+            const int col = q2 * 32 + i4 * 4 + t;
+            const float x = fmaf(f[q2][i4 * 4 + t], c, -lv[t]);
+            f[q2][i4 * 4 + t] = (col >= qlim) ? ex2(x) : 0.f;
           }
         }
 #pragma unroll
-        for (int i2 = 0; i2 < 16; ++i2) pk[i2] = pack_bf16(f[q4][2 * i2], f[q4][2 * i2 + 1]);
-        tmem_st16(lane_base + kTmS + q4 * 16, pk);
+        for (int i2 = 0; i2 < 16; ++i2) pk[i2] = pack_bf16(f[q2][2 * i2], f[q2][2 * i2 + 1]);
+        tmem_st16(tSh + q2 * 16, pk);
       }
-      // dS^T = P^T (dP^T - D[q]) into the first 64 columns of dP^T's region
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(2));  // P^T_i is in TMEM: dV may start
+      got = __all_sync(0xffffffffu, mbar_wait(bar(5), ii & 1, abort_flag));
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // dS^T = P^T (dP^T - D[q]) into the first 32 columns of this half's dP^T
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q2 = 0; q2 < 2; ++q2) {
         uint32_t dp[32];
-        tmem_ld32(lane_base + kTmDP + q4 * 32, dp);
+        tmem_ld32(tDPh + q2 * 32, dp);
         tmem_ld_wait(dp);
         uint32_t pk[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(Ds + q4 * 32 + i4 * 4);
+          const float4 d4 = *reinterpret_cast<const float4*>(Ds + q2 * 32 + i4 * 4);
           const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
           for (int t = 0; t < 4; t += 2) {
             const int e = i4 * 4 + t;
-            const float a = f[q4][e] * (__uint_as_float(dp[e]) - dv[t]);
-            const float b = f[q4][e + 1] * (__uint_as_float(dp[e + 1]) - dv[t + 1]);
+            const float a = f[q2][e] * (__uint_as_float(dp[e]) - dv[t]);
+            const float b = f[q2][e + 1] * (__uint_as_float(dp[e + 1]) - dv[t + 1]);
             pk[e / 2] = pack_bf16(a, b);
           }
         }
-        tmem_st16(lane_base + kTmDP + q4 * 16, pk);
+        tmem_st16(tDPh + q2 * 16, pk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(2));
+      mbar_arrive(bar(6));  // dS^T_i is in TMEM: dK may start
     }
     if (!ok) report_wait_failure(abort_flag, 1u);
     if (ok && nq > 0) {
@@ -579,12 +635,12 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const bool store = key < p.Nk;
         const size_t grow = static_cast<size_t>(bh) * p.Nk + key;
-        uint4* const outv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dv) + grow * D);
-        uint4* const outk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dk) + grow * D);
+        uint4* const outv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dv) + grow * D + h * (D / 2));
+        uint4* const outk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dk) + grow * D + h * (D / 2));
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 64; ++cc) {
           uint32_t o[32];
-          tmem_ld32(lane_base + kTmDV + cc * 32, o);
+          tmem_ld32(lane_base + kTmDV + h * (D / 2) + cc * 32, o);
           tmem_ld_wait(o);
           uint32_t w[16];
 #pragma unroll
@@ -593,7 +649,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) outv[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
           }
-          tmem_ld32(lane_base + kTmDK + cc * 32, o);
+          tmem_ld32(lane_base + kTmDK + h * (D / 2) + cc * 32, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
@@ -608,7 +664,7 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
