@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(320, 1)
     const int row = row0 + row_local;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const float c = p.scale_log2;
-    const float NEG_INF = -__int_as_float(0x7f800000), POS_INF = __int_as_float(0x7f800000);
+    const float POS_INF = __int_as_float(0x7f800000);
     const bool valid = row < p.Nq;
     const size_t grow = static_cast<size_t>(bh) * p.Nq + row;
     // D = rowsum(dO * O) in fp32, L = LSE * log2(e); padding rows: P = 0.

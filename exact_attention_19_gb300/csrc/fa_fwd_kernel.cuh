@@ -46,7 +46,7 @@ struct FwdParams {
   int Nq, Nk;
   int n_pairs;        // ceil(Nq / 256): query-tile pairs per (b, h)
   float scale_log2;   // scale * log2(e)
-  // MASKED only: key j is visible to query row i iff
+  // window mask only: key j is visible to query row i iff
   //   i + diag_off - win_left <= j <= i + diag_off + win_right  (a negative bound: unbounded)
   int win_left, win_right, diag_off;
   // split-KV only: CTAs per pair, K/V tiles per split, and the partial results
@@ -153,7 +153,6 @@ __global__ void __launch_bounds__(320, 1)
   }
   const int bh = cta / p.n_pairs;
   int pair = cta % p.n_pairs;
-  constexpr bool MASKED = MASK != kMaskNone;
   if (MASK == kMaskCausal) pair = p.n_pairs - 1 - pair;  // heaviest pair of each head first
   const int n_kv_all = (p.Nk + C::kBN - 1) / C::kBN;
   const int kv_lo = SPLIT ? split * p.split_tiles : 0;  // this CTA's slice of K/V tiles

@@ -188,13 +188,15 @@ const char* fa_strerror(int status);
 int fa_version(void);
 
 /*
- * fa_fwd_status -- synchronise `stream`, then report whether any fa_fwd kernel
- * on the current device gave up on a wait (FA_ERR_TIMEOUT) since the last
- * clear.  Every wait inside the kernel is bounded (about 2 s); a wait that
- * runs out records the failing role in the device status word, the CTA drains
- * its in-flight copies and MMAs, frees its tensor memory and exits.  *detail
- * (optional) receives the raw status word.  clear != 0 resets the word.
- * Returns FA_OK, FA_ERR_TIMEOUT, or FA_ERR_LAUNCH if synchronisation failed.
+ * fa_fwd_status -- synchronise `stream`, then report whether any kernel of
+ * this library (forward, split-KV, backward) on the current device gave up on
+ * a wait (FA_ERR_TIMEOUT) since the last clear.  Every wait inside the kernels
+ * is bounded (about 2 s); a wait that runs out records the failing role in the
+ * device status word (bit 0, and bits 8.. = 1 softmax/compute, 2 producer,
+ * 4 MMA issuer, 8 epilogue), the CTA drains its in-flight copies and MMAs,
+ * frees its tensor memory and exits.  *detail (optional) receives the raw
+ * status word.  clear != 0 resets the word.  Returns FA_OK, FA_ERR_TIMEOUT, or
+ * FA_ERR_LAUNCH if synchronisation failed.
  */
 int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear);
 
