@@ -41,6 +41,7 @@ EncodeTiledFn encode_fn() {
 // shared-memory opt-in.  0 = not yet, 1 = ready, -1 = unsupported device.
 std::atomic<int> g_dev_state[kMaxDevices];
 int g_dev_sms[kMaxDevices];  // multiprocessor count, valid once the state is 1
+long long g_dev_l2[kMaxDevices];  // L2 bytes, valid once the state is 1
 
 int g_dev_sms_or(int dev, int fallback) {
   return (dev >= 0 && dev < kMaxDevices && g_dev_sms[dev] > 0) ? g_dev_sms[dev] : fallback;
@@ -95,6 +96,9 @@ int prepare_device(int dev) {
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return FA_ERR_LAUNCH;
   g_dev_sms[dev] = sms;
+  int l2 = 0;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess || l2 <= 0) return FA_ERR_LAUNCH;
+  g_dev_l2[dev] = l2;
   if (!set_smem_attrs<64>() || !set_smem_attrs<128>() || !set_bwd_smem_attrs<64>() || !set_bwd_smem_attrs<128>())
     return FA_ERR_LAUNCH;
   g_dev_state[dev].store(1, std::memory_order_release);
@@ -204,6 +208,10 @@ int prepare_call(const void* q, const void* k, const void* v, void* o, float* ls
   p->o_part = nullptr;
   p->lse_part = nullptr;
   p->rows = BH * Nq;
+  // heads per causal scheduling group: their K and V fill at most half the L2
+  const long long kv_head_bytes = 4ll * Nk * d;
+  const long long group = (g_dev_l2[dev] / 2) / (kv_head_bytes > 0 ? kv_head_bytes : 1);
+  p->lpt_group = static_cast<int>(group < 1 ? 1 : (group > BH ? BH : group));
   *dev_out = dev;
   return FA_OK;
 }

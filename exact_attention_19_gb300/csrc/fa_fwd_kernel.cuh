@@ -51,6 +51,8 @@ struct FwdParams {
   int win_left, win_right, diag_off;
   // split-KV only: CTAs per pair, K/V tiles per split, and the partial results
   int n_splits, split_tiles;
+  // causal only: heads per scheduling group (their K/V fit in half the L2)
+  int lpt_group;
   float* o_part;      // fp32 [n_splits, BH * Nq, D], each slice normalised by its own l
   float* lse_part;    // fp32 [n_splits, BH * Nq], m_bar + log2(l) in base-2 scaled units
   long long rows;     // BH * Nq
@@ -151,9 +153,22 @@ __global__ void __launch_bounds__(320, 1)
     split = cta % p.n_splits;
     cta /= p.n_splits;
   }
-  const int bh = cta / p.n_pairs;
+  int bh = cta / p.n_pairs;
   int pair = cta % p.n_pairs;
-  if (MASK == kMaskCausal) pair = p.n_pairs - 1 - pair;  // heaviest pair of each head first
+  if (MASK == kMaskCausal) {
+    // Causal pairs differ in work (pair i sees 2i + 2 K/V tiles).  Heads are
+    // taken in groups whose K/V fit in half the L2; inside a group the
+    // heaviest pairs of all its heads run first, so a group's last wave holds
+    // its lightest pairs (longest-processing-time-first order), while the
+    // CTAs in flight at any time share the K/V tiles of a few heads.
+    const int n_bh = static_cast<int>(gridDim.x / (SPLIT ? p.n_splits : 1)) / p.n_pairs;
+    const int per_group = p.lpt_group * p.n_pairs;
+    const int g0 = (cta / per_group) * p.lpt_group;
+    const int g_heads = min(p.lpt_group, n_bh - g0);
+    const int within = cta - (cta / per_group) * per_group;
+    bh = g0 + within % g_heads;
+    pair = p.n_pairs - 1 - within / g_heads;
+  }
   const int n_kv_all = (p.Nk + C::kBN - 1) / C::kBN;
   const int kv_lo = SPLIT ? split * p.split_tiles : 0;  // this CTA's slice of K/V tiles
   const int kv_hi = SPLIT ? min(n_kv_all, kv_lo + p.split_tiles) : n_kv_all;
