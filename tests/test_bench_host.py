@@ -95,3 +95,19 @@ def test_reference_arm_other_ranks_silent(monkeypatch):
     with contextlib.redirect_stdout(buf):
         rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3"])
     assert rc == 0 and buf.getvalue() == ""
+
+
+def test_roofline_bound_follows_intensity():
+    import synth
+
+    peak, hbm = 1891.4, 6789.0
+    # the long workload sits far above the ridge (about 279 FLOP per byte): tensor-bound
+    w = synth.WORKLOADS["long_8192_d128"]
+    r = bench.roofline_entry(w.flops, w.algorithmic_bytes, 1500.0, 400.0, peak, hbm)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and abs(r["frac"] - 1500.0 / peak) < 1e-12
+    # the single-head N = 256 case (127 FLOP per byte) and the GPT-2 shape (254) are below it
+    for name in ("single_head_256_d64", "gpt2_small_causal_1024_d64"):
+        w = synth.WORKLOADS[name]
+        r = bench.roofline_entry(w.flops, w.algorithmic_bytes, 1.0, 50.0, peak, hbm)
+        assert r["bound"] == "hbm" and r["unit"] == "GB/s" and abs(r["frac"] - 50.0 / hbm) < 1e-12
+        assert r["intensity_flop_per_byte"] < r["ridge_flop_per_byte"]
