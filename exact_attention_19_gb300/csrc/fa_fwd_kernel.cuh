@@ -51,7 +51,7 @@ struct FwdParams {
   int win_left, win_right, diag_off;
   // split-KV only: CTAs per pair, K/V tiles per split, and the partial results
   int n_splits, split_tiles;
-  // causal only: heads per scheduling group (their K/V fit in half the L2)
+  // causal only: heads per scheduling group (their K/V fit in a quarter of the L2)
   int lpt_group;
   float* o_part;      // fp32 [n_splits, BH * Nq, D], each slice normalised by its own l
   float* lse_part;    // fp32 [n_splits, BH * Nq], m_bar + log2(l) in base-2 scaled units
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(320, 1)
   int pair = cta % p.n_pairs;
   if (MASK == kMaskCausal) {
     // Causal pairs differ in work (pair i sees 2i + 2 K/V tiles).  Heads are
-    // taken in groups whose K/V fit in half the L2; inside a group the
+    // taken in groups whose K/V fit in a quarter of the L2; inside a group the
     // heaviest pairs of all its heads run first, so a group's last wave holds
     // its lightest pairs (longest-processing-time-first order), while the
     // CTAs in flight at any time share the K/V tiles of a few heads.
