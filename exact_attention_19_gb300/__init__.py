@@ -1,10 +1,12 @@
-"""GB300-native fused exact-attention forward (sm_103a).
+"""GB300-native fused exact attention (sm_103a): forward, split-KV, sliding
+window and backward.
 
 Thin ctypes binding over ``libfa_gb300.so`` (C ABI in ``include/fa.h``):
 argument marshalling only, every step of the computation runs in the CUDA
-kernel.  PyTorch supplies device memory and streams.
+kernels.  PyTorch supplies device memory and streams.
 
     o, lse = fwd(q, k, v, causal=False)          # torch bf16 [B, H, N, d]
+    dq, dk, dv = bwd(q, k, v, o, lse, do, causal=False)
     fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, Nq, Nk, d, scale, causal, stream)
 
 There is no fallback: if the library cannot be loaded, every call raises.
@@ -15,9 +17,13 @@ import ctypes
 import math
 import os
 
-__all__ = ["FaError", "fa_fwd", "fa_fwd_window", "fa_fwd_splitkv", "fa_bwd", "fa_bwd_workspace_bytes", "bwd", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
-           "fa_splitkv_heuristic", "NOALLOC_SCRATCH_BYTES",
-           "fa_strerror", "fa_version", "fa_fwd_status", "fwd", "library_path", "load", "STATUS"]
+__all__ = [
+    "FaError", "STATUS", "NOALLOC_SCRATCH_BYTES", "library_path", "load",
+    "fwd", "bwd",
+    "fa_fwd", "fa_fwd_window", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
+    "fa_splitkv_heuristic", "fa_bwd", "fa_bwd_workspace_bytes", "fa_probe_exp2", "fa_fwd_status",
+    "fa_strerror", "fa_version",
+]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libfa_gb300.so")
@@ -258,6 +264,10 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    for name, t, like in (("dq", dq, q), ("dk", dk, k), ("dv", dv, v)):
+        if (not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or not t.is_cuda or
+                not t.is_contiguous() or t.shape != like.shape):
+            raise ValueError(f"{name} must be a contiguous CUDA bf16 tensor shaped like {tuple(like.shape)}")
     need = fa_bwd_workspace_bytes(B, H, Nq)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
