@@ -140,3 +140,17 @@ def test_bwd_stress_sampled_dq():
     dq_ref = backward.attention_bwd_dq_rows(q, k, v, do, rows, w.scale, True)
     assert _err(dq.reshape(-1, w.d)[rows], dq_ref) <= TOL
     assert np.all(np.isfinite(dk)) and np.all(np.isfinite(dv))
+
+
+def test_bwd_binding_rejects_bad_gradient_buffers():
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    t = torch.zeros((1, 2, 130, 64), dtype=torch.bfloat16, device="cuda")
+    o, lse = fa.fwd(t, t, t)
+    with pytest.raises(ValueError):
+        fa.bwd(t, t, t, o, lse, t, dq=torch.empty((1, 2, 129, 64), dtype=torch.bfloat16, device="cuda"))
+    with pytest.raises(ValueError):
+        fa.bwd(t, t, t, o, lse, t, dk=torch.empty((1, 2, 130, 64), dtype=torch.float32, device="cuda"))
+    torch.cuda.synchronize()
