@@ -86,6 +86,22 @@ def roofline_entry(flops, algo_bytes, achieved_tflops, achieved_gbs, peak_tflops
     return out
 
 
+def e2e_entry(pipe_value, pipe_ms, serial_value, serial_ms, h2d_bytes, d2h_bytes, steps):
+    """End-to-end line: the faster of the two ways of running the steps (both
+    move every step's inputs in and results out inside the timed region), with
+    both figures kept."""
+    use_pipe = not (serial_value > pipe_value)  # NaN-safe: a missing serial run picks the pipelined one
+    return {"value": pipe_value if use_pipe else serial_value, "unit": UNIT,
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+            "ms_per_step": pipe_ms if use_pipe else serial_ms, "steps": steps,
+            "mode": "pipelined" if use_pipe else "serial",
+            "pipelined_value": pipe_value, "pipelined_ms_per_step": pipe_ms,
+            "serial_value": serial_value, "serial_ms_per_step": serial_ms,
+            "how": "pinned host inputs copied in and O, LSE read back every step; serial: copies and kernel on "
+                   "one stream; pipelined: two device buffer sets, copies on two copy streams overlapping the "
+                   "previous step's kernel"}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -357,41 +373,86 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
         raise RuntimeError(f"kernel reported a wait timeout (status {word:#x})")
 
     # ---- end-to-end through the public API with host buffers ----------------
-    o_host = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
-    lse_host = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
-    qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-
-    def e2e_step():
-        qd.copy_(q_p, non_blocking=True)
-        kd.copy_(k_p, non_blocking=True)
-        vd.copy_(v_p, non_blocking=True)
-        fa.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, n_splits=n_splits,
-               workspace=workspace)
-        o_host.copy_(o, non_blocking=True)
-        lse_host.copy_(lse, non_blocking=True)
-
+    # Every step copies its inputs from pinned host memory, runs fa.fwd and
+    # reads O and LSE back into pinned host memory.  Serial: all on one stream.
+    # Pipelined (the reported e2e): two device buffer sets, host->device copies
+    # on one copy stream and device->host reads on another, so step k+1's
+    # inputs travel while step k computes; each step still moves its own bytes.
+    o_host = [torch.empty(o.shape, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    lse_host = [torch.empty(lse.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     e2e_steps = max(1, min(args.steps, 50))
-    e2e_ms = float("nan")
+    e2e_ms = e2e_serial_ms = float("nan")
     if not args.no_e2e:
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_serial_step():
+            qd.copy_(q_p, non_blocking=True)
+            kd.copy_(k_p, non_blocking=True)
+            vd.copy_(v_p, non_blocking=True)
+            fa.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, n_splits=n_splits,
+                   workspace=workspace)
+            o_host[0].copy_(o, non_blocking=True)
+            lse_host[0].copy_(lse, non_blocking=True)
+
+        sets = [(qd, kd, vd, o, lse),
+                (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(o),
+                 torch.empty_like(lse))]
+        h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_kernel = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+
+        def e2e_pipelined(n):
+            for i in range(n):
+                b = i & 1
+                qb, kb, vb, ob, lb = sets[b]
+                if i >= 2:
+                    h2d_stream.wait_event(ev_kernel[b])  # step i-2 has finished reading this input set
+                with torch.cuda.stream(h2d_stream):
+                    qb.copy_(q_p, non_blocking=True)
+                    kb.copy_(k_p, non_blocking=True)
+                    vb.copy_(v_p, non_blocking=True)
+                ev_in[b].record(h2d_stream)
+                stream.wait_event(ev_in[b])
+                if i >= 2:
+                    stream.wait_event(ev_out[b])  # step i-2's outputs have been read back
+                fa.fwd(qb, kb, vb, causal=w.causal, scale=w.scale, out=ob, lse=lb, stream=stream,
+                       n_splits=n_splits, workspace=workspace)
+                ev_kernel[b].record(stream)
+                d2h_stream.wait_event(ev_kernel[b])
+                with torch.cuda.stream(d2h_stream):
+                    o_host[b].copy_(ob, non_blocking=True)
+                    lse_host[b].copy_(lb, non_blocking=True)
+                ev_out[b].record(d2h_stream)
+            stream.wait_stream(h2d_stream)
+            stream.wait_stream(d2h_stream)
+
+        def timed(fn):
+            barrier()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            barrier()
+            return e0.elapsed_time(e1) / e2e_steps
+
         for _ in range(min(args.warmup, 3)):
-            e2e_step()
-        barrier()
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        barrier()
+            e2e_serial_step()
+        e2e_pipelined(min(args.warmup, 3))
+        e2e_serial_ms = timed(lambda: [e2e_serial_step() for _ in range(e2e_steps)])
+        e2e_ms = timed(lambda: e2e_pipelined(e2e_steps))
+        st, word = fa.fa_fwd_status(None, clear=True)
+        if st != 0:
+            raise RuntimeError(f"kernel reported a wait timeout in the end-to-end run (status {word:#x})")
 
     # ---- max over ranks -------------------------------------------------------
-    t_max_elapsed, t_max_e2e = max_over_ranks([elapsed, e2e_ms], dist, dev)
+    t_max_elapsed, t_max_e2e, t_max_e2e_serial = max_over_ranks([elapsed, e2e_ms, e2e_serial_ms], dist, dev)
     times = [t_max_elapsed] * world
-    e2e_times = [t_max_e2e] * world
     value, t_max = aggregate(times, [w.flops * args.steps] * world)
-    e2e_value, _ = aggregate(e2e_times, [w.flops] * world)
+    e2e_value, _ = aggregate([t_max_e2e] * world, [w.flops] * world)
+    e2e_serial_value, _ = aggregate([t_max_e2e_serial] * world, [w.flops] * world)
     ms_per_step = t_max / args.steps
 
     if rank != 0:
@@ -434,9 +495,8 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(config_of(w, l2_note), n_splits=n_splits),
         "roofline": roofline, "mufu_roofline": mufu, "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(in_bytes),
-                "d2h_bytes_per_step": int(2 * o.numel() + 4 * lse.numel()), "ms_per_step": e2e_ms,
-                "steps": e2e_steps},
+        "e2e": e2e_entry(e2e_value, e2e_ms, e2e_serial_value, e2e_serial_ms, int(in_bytes),
+                         int(2 * o.numel() + 4 * lse.numel()), e2e_steps),
         "gpu_launches": args.steps * launches_per_step, "clocks": clocks,
         "pct_of_peak": 100.0 * achieved / peak,  # of the dense bf16 peak, whatever the binding roofline
     }

@@ -111,3 +111,11 @@ def test_roofline_bound_follows_intensity():
         r = bench.roofline_entry(w.flops, w.algorithmic_bytes, 1.0, 50.0, peak, hbm)
         assert r["bound"] == "hbm" and r["unit"] == "GB/s" and abs(r["frac"] - 50.0 / hbm) < 1e-12
         assert r["intensity_flop_per_byte"] < r["ridge_flop_per_byte"]
+
+
+def test_e2e_entry_reports_the_faster_mode_and_both_figures():
+    e = bench.e2e_entry(1000.0, 4.0, 500.0, 8.0, 100, 10, 5)
+    assert e["mode"] == "pipelined" and e["value"] == 1000.0 and e["ms_per_step"] == 4.0
+    assert e["serial_value"] == 500.0 and e["h2d_bytes_per_step"] == 100 and e["d2h_bytes_per_step"] == 10
+    e = bench.e2e_entry(50.0, 0.08, 88.0, 0.05, 100, 10, 5)
+    assert e["mode"] == "serial" and e["value"] == 88.0 and e["pipelined_value"] == 50.0
