@@ -21,7 +21,8 @@ __all__ = [
     "FaError", "STATUS", "NOALLOC_SCRATCH_BYTES", "library_path", "load",
     "fwd", "bwd",
     "fa_fwd", "fa_fwd_window", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
-    "fa_splitkv_heuristic", "fa_bwd", "fa_bwd_workspace_bytes", "fa_probe_exp2", "fa_fwd_status",
+    "fa_splitkv_heuristic", "fa_bwd", "fa_bwd_workspace_bytes", "fa_probe_exp2", "fa_selftest_wait",
+    "fa_fwd_status",
     "fa_strerror", "fa_version",
 ]
 
@@ -68,6 +69,8 @@ def load():
         lib.fa_fwd_status.restype = i32
         lib.fa_probe_exp2.argtypes = [i32, ctypes.POINTER(ctypes.c_double), vp]
         lib.fa_probe_exp2.restype = i32
+        lib.fa_selftest_wait.argtypes = [i32, ctypes.POINTER(ctypes.c_uint), ctypes.POINTER(ctypes.c_ulonglong), vp]
+        lib.fa_selftest_wait.restype = i32
         lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, vp,
                                        ctypes.c_size_t, vp]
         lib.fa_fwd_splitkv.restype = i32
@@ -164,6 +167,15 @@ def fa_probe_exp2(method: int = 0, stream=None) -> float:
     if st != 0:
         raise FaError(st, "fa_probe_exp2")
     return float(rate.value)
+
+
+def fa_selftest_wait(mode: int, stream=None):
+    """Run the bounded-wait self-test (0: time limit, 1: abort flag); returns (status word, wait ns)."""
+    word, ns = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+    st = int(load().fa_selftest_wait(int(mode), ctypes.byref(word), ctypes.byref(ns), stream))
+    if st != 0:
+        raise FaError(st, "fa_selftest_wait")
+    return int(word.value), int(ns.value)
 
 
 def _stream_handle(stream):

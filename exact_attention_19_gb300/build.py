@@ -1,8 +1,9 @@
 """Build libfa_gb300.so in-tree with nvcc (sm_103a only).
 
-Two translation units: fa_api.cu (the C-ABI front end with every forward,
-split-KV merge and backward kernel instantiation) and fa_probe.cu (the
-exp2-throughput probe), compiled in one nvcc call.
+Three translation units: fa_api.cu (the C-ABI front end with every forward,
+split-KV merge and backward kernel instantiation), fa_probe.cu (the
+exp2-throughput probe) and fa_selftest.cu (the bounded-wait self-test),
+compiled in one nvcc call.
 """
 from __future__ import annotations
 
@@ -17,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libfa_gb300.so")
-SOURCES = [os.path.join(CSRC, "fa_api.cu"), os.path.join(CSRC, "fa_probe.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("fa_api.cu", "fa_probe.cu", "fa_selftest.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_ptx.cuh", "fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh")] + [
     os.path.join(INCLUDE, "fa.h")]
 

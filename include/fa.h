@@ -218,6 +218,23 @@ int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear);
  */
 int fa_probe_exp2(int method, double* per_clk_sm, cudaStream_t stream);
 
+/*
+ * fa_selftest_wait -- exercise the bounded wait that every kernel of this
+ * library uses, without any fault: one CTA waits on an mbarrier phase that
+ * nothing completes.  Not an operation of the pages.
+ *
+ * mode 0: the wait must give up when its time limit (about 2 s) runs out;
+ * mode 1: another warp raises the CTA's abort flag after about 1 ms and the
+ *         wait must give up on it at once.
+ * word     receives the self-test's status word: bit 0 set when the wait gave
+ *          up; bits 8.. = 1 (time limit) or 2 (abort flag).
+ * wait_ns  receives how long the wait lasted, in nanoseconds.
+ * Synchronises `stream`; the device status word of the other kernels is not
+ * touched.  Returns FA_ERR_NULL, FA_ERR_SHAPE (mode), FA_ERR_DEVICE or
+ * FA_ERR_LAUNCH; the outputs are written only on FA_OK.
+ */
+int fa_selftest_wait(int mode, unsigned int* word, unsigned long long* wait_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

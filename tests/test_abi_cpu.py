@@ -49,6 +49,14 @@ def test_version_and_strerror(lib):
     assert fa.fa_strerror(12345) == "unknown status"
 
 
+def test_selftest_rejects_bad_arguments(lib):
+    import ctypes
+
+    w, n = ctypes.c_uint(), ctypes.c_ulonglong()
+    assert lib.fa_selftest_wait(0, None, ctypes.byref(n), None) == 1  # FA_ERR_NULL
+    assert lib.fa_selftest_wait(2, ctypes.byref(w), ctypes.byref(n), None) == 3  # FA_ERR_SHAPE
+
+
 def test_probe_rejects_bad_arguments(lib):
     import ctypes
 
