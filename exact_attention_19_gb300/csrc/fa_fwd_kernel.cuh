@@ -296,7 +296,7 @@ __global__ void __launch_bounds__(320, 1)
       // every barrier check of the first half gathered in one place (each
       // check behind queued MMAs costs a pipe bubble, consecutive ones cost one).
       // A tile whose range starts after J0 gets its first S when j + 1 enters it.
-      for (int jj = 0; ok && jj < n_max; ++jj) {
+      auto general = [&](int jj) -> bool {
         const int j = J0 + jj;
         const int iv = 2 * jj + 1, ik = 2 * jj + 2;  // ring items of V_j and K_{j+1}
         const int sv = iv % C::kRing, sk = ik % C::kRing;
@@ -308,9 +308,9 @@ __global__ void __launch_bounds__(320, 1)
           const bool b = !has_next || mbar_try_wait(full(sk), (ik / C::kRing) & 1);
           const bool c = !pv0 || mbar_try_wait(bar(kBarP + 0), (j - jlo[0]) & 1);
           if (!(a && b && c)) {
-            if (!(ok = wait_item(iv))) break;
-            if (has_next && !(ok = wait_item(ik))) break;
-            if (pv0 && !(ok = mbar_wait(bar(kBarP + 0), (j - jlo[0]) & 1, abort_flag))) break;
+            if (!wait_item(iv)) return false;
+            if (has_next && !wait_item(ik)) return false;
+            if (pv0 && !mbar_wait(bar(kBarP + 0), (j - jlo[0]) & 1, abort_flag)) return false;
           }
         }
         tc_fence_after();
@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(320, 1)
           mma_commit(bar(kBarS + 0));
         }
         if (pv1) {
-          if (!(ok = mbar_wait(bar(kBarP + 1), (j - jlo[1]) & 1, abort_flag))) break;
+          if (!mbar_wait(bar(kBarP + 1), (j - jlo[1]) & 1, abort_flag)) return false;
           tc_fence_after();
           gemm2(1, sv, j > jlo[1]);
           if (j == jhi[1] - 1) mma_commit(bar(kBarO + 1));
@@ -334,7 +334,56 @@ __global__ void __launch_bounds__(320, 1)
           mma_commit(bar(kBarS + 1));
         }
         if (has_next) mma_commit(empty(sk));
+        return true;
+      };
+      // The steady state: K/V tiles j with j - 1, j and j + 1 in both query
+      // tiles' ranges, so every product of the tile is issued and none is the
+      // last of its tile.  The same issue order without a branch around the
+      // MMAs: a barrier test by this thread completes only after its queued
+      // MMAs, and a branch next to it costs the pipe about 20 cycles per MMA.
+      auto steady = [&](int jj) -> bool {
+        const int j = J0 + jj;
+        const int iv = 2 * jj + 1, ik = 2 * jj + 2;
+        const int sv = iv % C::kRing, sk = ik % C::kRing;
+        const uint32_t phv = (iv / C::kRing) & 1, phk = (ik / C::kRing) & 1;
+        const uint32_t ph0 = (j - jlo[0]) & 1, ph1 = (j - jlo[1]) & 1;
+        const bool a = mbar_try_wait(full(sv), phv);
+        const bool b = mbar_try_wait(full(sk), phk);
+        const bool c = mbar_try_wait(bar(kBarP + 0), ph0);
+        if (!(a && b && c)) {
+          if (!mbar_wait(full(sv), phv, abort_flag) || !mbar_wait(full(sk), phk, abort_flag) ||
+              !mbar_wait(bar(kBarP + 0), ph0, abort_flag))
+            return false;
+        }
+        tc_fence_after();
+        gemm2(0, sv, true);
+        gemm1(0, sk);
+        mma_commit(bar(kBarS + 0));
+        if (!mbar_try_wait(bar(kBarP + 1), ph1)) {
+          if (!mbar_wait(bar(kBarP + 1), ph1, abort_flag)) return false;
+        }
+        tc_fence_after();
+        gemm2(1, sv, true);
+        mma_commit(empty(sv));
+        gemm1(1, sk);
+        mma_commit(bar(kBarS + 1));
+        mma_commit(empty(sk));
+        return true;
+      };
+      // steady range [s_lo, s_hi) of jj; the tiles before and after it take
+      // the general body
+      int s_lo = n_max, s_hi = n_max;
+      if (nkv[0] > 0 && nkv[1] > 0) {
+        const int lo = max(jlo[0], jlo[1]) + 1 - J0, hi = min(jhi[0], jhi[1]) - 1 - J0;
+        if (lo < hi) {
+          s_lo = lo;
+          s_hi = hi;
+        }
       }
+      int jj = 0;
+      for (; ok && jj < s_lo; ++jj) ok = general(jj);
+      for (; ok && jj < s_hi; ++jj) ok = steady(jj);
+      for (; ok && jj < n_max; ++jj) ok = general(jj);
       if (!ok) report_wait_failure(abort_flag, 4u);
       // Drain: every MMA issued so far has completed once this barrier flips.
       mma_commit(bar(kBarDrain));
