@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(320, 1)
       // dP_j into dS_j: S_{j+1} may overwrite S once it has been read (P stays
       // in registers), and dP_{j+1} goes to the other dP buffer, whose last
       // reader (dQ += dS_{j-1} K_{j-1}) was issued before it.
-      for (int j = 0; ok && j < nkv; ++j) {
+      auto general = [&](int j) -> bool {
         const bool has_next = j + 1 < nkv;
         const int sk = (2 * j + 1) % R;
         if (has_next) {
@@ -211,9 +211,7 @@ __global__ void __launch_bounds__(320, 1)
           const bool b = mbar_try_wait(full(ik % R), (ik / R) & 1);
           const bool c = mbar_try_wait(full(iv % R), (iv / R) & 1);
           if (!(a && b && c)) {
-            if (!(ok = mbar_wait(bar(3), j & 1, abort_flag))) break;
-            if (!(ok = wait_item(ik))) break;
-            if (!(ok = wait_item(iv))) break;
+            if (!mbar_wait(bar(3), j & 1, abort_flag) || !wait_item(ik) || !wait_item(iv)) return false;
           }
           tc_fence_after();
           score(dQd, ik % R, kTmS);
@@ -222,12 +220,46 @@ __global__ void __launch_bounds__(320, 1)
           mma_commit(bar(2));
           mma_commit(empty(iv % R));  // V_{j+1} is done
         }
-        if (!(ok = mbar_wait(bar(4), j & 1, abort_flag))) break;
+        if (!mbar_wait(bar(4), j & 1, abort_flag)) return false;
         tc_fence_after();
         acc_dq(sk, kTmDP + (j & 1) * 128, j > 0);
         mma_commit(empty(sk));  // K_j is done
         if (j == nkv - 1) mma_commit(bar(5));
-      }
+        return true;
+      };
+      // Tiles 1 .. nkv-2: the same products with no branch around the MMAs (a
+      // branch next to a barrier test of this thread costs the pipe about 20
+      // cycles per MMA; the test itself waits for the MMAs already queued).
+      auto steady = [&](int j) -> bool {
+        const int sk = (2 * j + 1) % R;
+        const int iv = 2 * j + 2, ik = 2 * j + 3;
+        const uint32_t p3 = j & 1, pk = (ik / R) & 1, pv = (iv / R) & 1;
+        const bool a = mbar_try_wait(bar(3), p3);
+        const bool b = mbar_try_wait(full(ik % R), pk);
+        const bool c = mbar_try_wait(full(iv % R), pv);
+        if (!(a && b && c)) {
+          if (!mbar_wait(bar(3), p3, abort_flag) || !mbar_wait(full(ik % R), pk, abort_flag) ||
+              !mbar_wait(full(iv % R), pv, abort_flag))
+            return false;
+        }
+        tc_fence_after();
+        score(dQd, ik % R, kTmS);
+        mma_commit(bar(1));
+        score(dDOd, iv % R, kTmDP + ((j + 1) & 1) * 128);
+        mma_commit(bar(2));
+        mma_commit(empty(iv % R));  // V_{j+1} is done
+        if (!mbar_try_wait(bar(4), p3)) {
+          if (!mbar_wait(bar(4), p3, abort_flag)) return false;
+        }
+        tc_fence_after();
+        acc_dq(sk, kTmDP + (j & 1) * 128, true);
+        mma_commit(empty(sk));  // K_j is done
+        return true;
+      };
+      int j = 0;
+      if (ok && nkv > 0) ok = general(j++);
+      for (; ok && j < nkv - 1; ++j) ok = steady(j);
+      for (; ok && j < nkv; ++j) ok = general(j);
       if (!ok) report_wait_failure(abort_flag, 4u);
       mma_commit(bar(6));
       mbar_wait(bar(6), 0, nullptr);
@@ -500,15 +532,15 @@ __global__ void __launch_bounds__(320, 1)
       // exponentiate S^T_{i+1}: S^T_{i+1} overwrites P^T_i only after the dV
       // product that reads it (issued first), dP^T_{i+1} overwrites dS^T_i only
       // after the dK product.
-      for (int ii = 0; ok && ii < nq; ++ii) {
+      auto general = [&](int ii) -> bool {
         const int iq = 2 * ii, ido = 2 * ii + 1;
         const bool has_next = ii + 1 < nq;
         {
           const bool a = mbar_try_wait(bar(2), ii & 1);
           const bool b = !has_next || mbar_try_wait(full((iq + 2) % R), ((iq + 2) / R) & 1);
           if (!(a && b)) {
-            if (!(ok = mbar_wait(bar(2), ii & 1, abort_flag))) break;
-            if (has_next && !(ok = wait_item(iq + 2))) break;
+            if (!mbar_wait(bar(2), ii & 1, abort_flag)) return false;
+            if (has_next && !wait_item(iq + 2)) return false;
           }
         }
         tc_fence_after();
@@ -522,8 +554,8 @@ __global__ void __launch_bounds__(320, 1)
           const bool a = mbar_try_wait(bar(6), ii & 1);
           const bool b = !has_next || mbar_try_wait(full((ido + 2) % R), ((ido + 2) / R) & 1);
           if (!(a && b)) {
-            if (!(ok = mbar_wait(bar(6), ii & 1, abort_flag))) break;
-            if (has_next && !(ok = wait_item(ido + 2))) break;
+            if (!mbar_wait(bar(6), ii & 1, abort_flag)) return false;
+            if (has_next && !wait_item(ido + 2)) return false;
           }
         }
         tc_fence_after();
@@ -533,7 +565,44 @@ __global__ void __launch_bounds__(320, 1)
           score(dVd, (ido + 2) % R, kTmDP);  // dP^T_{i+1}
           mma_commit(bar(5));
         }
-      }
+        return true;
+      };
+      // Query tiles 1 .. nq-2: the same products with no branch around the
+      // MMAs (a branch next to a barrier test of this thread costs the pipe
+      // about 20 cycles per MMA).
+      auto steady = [&](int ii) -> bool {
+        const int iq = 2 * ii, ido = 2 * ii + 1;
+        const uint32_t pb = ii & 1, pq = ((iq + 2) / R) & 1, pd = ((ido + 2) / R) & 1;
+        {
+          const bool a = mbar_try_wait(bar(2), pb);
+          const bool b = mbar_try_wait(full((iq + 2) % R), pq);
+          if (!(a && b)) {
+            if (!mbar_wait(bar(2), pb, abort_flag) || !mbar_wait(full((iq + 2) % R), pq, abort_flag)) return false;
+          }
+        }
+        tc_fence_after();
+        accum(kTmDV, kTmS, ido % R, true);  // dV += P^T dO_i
+        mma_commit(empty(ido % R));         // dO_i is done
+        score(dKd, (iq + 2) % R, kTmS);     // S^T_{i+1}
+        mma_commit(bar(1));
+        {
+          const bool a = mbar_try_wait(bar(6), pb);
+          const bool b = mbar_try_wait(full((ido + 2) % R), pd);
+          if (!(a && b)) {
+            if (!mbar_wait(bar(6), pb, abort_flag) || !mbar_wait(full((ido + 2) % R), pd, abort_flag)) return false;
+          }
+        }
+        tc_fence_after();
+        accum(kTmDK, kTmDP, iq % R, true);  // dK += dS^T Q_i
+        mma_commit(empty(iq % R));          // Q_i (and its L, D) is done
+        score(dVd, (ido + 2) % R, kTmDP);   // dP^T_{i+1}
+        mma_commit(bar(5));
+        return true;
+      };
+      int ii = 0;
+      if (ok && nq > 0) ok = general(ii++);
+      for (; ok && ii < nq - 1; ++ii) ok = steady(ii);
+      for (; ok && ii < nq; ++ii) ok = general(ii);
       if (ok) mma_commit(bar(3));
       if (!ok) report_wait_failure(abort_flag, 4u);
       mma_commit(bar(4));
