@@ -409,6 +409,16 @@ __global__ void __launch_bounds__(320, 1)
                        const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingKV;
+  // Ring slot and phase of item `it` (even: Q_i with its L and D, odd: dO_i; i = it / 2).
+  // Query tile i uses the slot pair i % (R/2), and Q and dO swap places each time a
+  // pair comes round again, so Q_{i+1} lands in the slot that dO_{i-1} left: dV_{i-1}
+  // frees it half an iteration before dK_{i-1} frees Q_{i-1}'s, and Q_{i+1} (needed
+  // first, by S^T_{i+1}) gets that much more time to arrive.
+  auto item_slot = [](int it) -> int {
+    const int i = it >> 1;
+    return 2 * (i % (R / 2)) + ((it & 1) ^ ((i / (R / 2)) & 1));
+  };
+  auto item_phase = [](int it) -> uint32_t { return static_cast<uint32_t>((it >> 1) / (R / 2)) & 1u; };
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -470,9 +480,9 @@ __global__ void __launch_bounds__(320, 1)
       int item = 0;
       bool ok = true;
       for (; item < 2 * nq; ++item) {  // Q_i (with its L, D), dO_i, ...
-        const int s = item % R;
+        const int s = item_slot(item);
         const int i = i0 + (item >> 1);
-        if (!(ok = mbar_wait(empty(s), ((item / R) & 1) ^ 1u, abort_flag))) break;
+        if (!(ok = mbar_wait(empty(s), item_phase(item) ^ 1u, abort_flag))) break;
         if (item & 1) {
           mbar_arrive_expect_tx(full(s), C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
@@ -489,7 +499,7 @@ __global__ void __launch_bounds__(320, 1)
       }
       if (!ok) report_wait_failure(abort_flag, 2u);
       if (*abort_flag) {
-        for (int it = max(0, item - R); it < item; ++it) mbar_wait(full(it % R), (it / R) & 1, nullptr);
+        for (int it = max(0, item - R); it < item; ++it) mbar_wait(full(item_slot(it)), item_phase(it), nullptr);
         mbar_wait(bar(0), 0, nullptr);
       }
     }
@@ -517,13 +527,13 @@ __global__ void __launch_bounds__(320, 1)
           mma_ts(tmem + dst, tmem + a_cols + (kk >> 2) * 64 + (kk & 3) * 8, dRingMN + slot_off(s) + ((kk * 2048) >> 4),
                  C::kIdescAcc, (acc_prev || kk > 0) ? 1u : 0u);
       };
-      auto wait_item = [&](int it) -> bool { return mbar_wait(full(it % R), (it / R) & 1, abort_flag); };
+      auto wait_item = [&](int it) -> bool { return mbar_wait(full(item_slot(it)), item_phase(it), abort_flag); };
       bool ok = mbar_wait(bar(0), 0, abort_flag) && wait_item(0) && wait_item(1);
       if (ok) {
         tc_fence_after();
-        score(dKd, 0, kTmS);
+        score(dKd, item_slot(0), kTmS);
         mma_commit(bar(1));
-        score(dVd, 1, kTmDP);
+        score(dVd, item_slot(1), kTmDP);
         mma_commit(bar(5));
       }
       // Per query tile i: [P^T_i written, Q_{i+1}] dV += P^T_i dO_i, S^T_{i+1};
@@ -537,32 +547,32 @@ __global__ void __launch_bounds__(320, 1)
         const bool has_next = ii + 1 < nq;
         {
           const bool a = mbar_try_wait(bar(2), ii & 1);
-          const bool b = !has_next || mbar_try_wait(full((iq + 2) % R), ((iq + 2) / R) & 1);
+          const bool b = !has_next || mbar_try_wait(full(item_slot(iq + 2)), item_phase(iq + 2));
           if (!(a && b)) {
             if (!mbar_wait(bar(2), ii & 1, abort_flag)) return false;
             if (has_next && !wait_item(iq + 2)) return false;
           }
         }
         tc_fence_after();
-        accum(kTmDV, kTmS, ido % R, ii > 0);  // dV += P^T dO_i
-        mma_commit(empty(ido % R));           // dO_i is done
+        accum(kTmDV, kTmS, item_slot(ido), ii > 0);  // dV += P^T dO_i
+        mma_commit(empty(item_slot(ido)));           // dO_i is done
         if (has_next) {
-          score(dKd, (iq + 2) % R, kTmS);  // S^T_{i+1}
+          score(dKd, item_slot(iq + 2), kTmS);  // S^T_{i+1}
           mma_commit(bar(1));
         }
         {
           const bool a = mbar_try_wait(bar(6), ii & 1);
-          const bool b = !has_next || mbar_try_wait(full((ido + 2) % R), ((ido + 2) / R) & 1);
+          const bool b = !has_next || mbar_try_wait(full(item_slot(ido + 2)), item_phase(ido + 2));
           if (!(a && b)) {
             if (!mbar_wait(bar(6), ii & 1, abort_flag)) return false;
             if (has_next && !wait_item(ido + 2)) return false;
           }
         }
         tc_fence_after();
-        accum(kTmDK, kTmDP, iq % R, ii > 0);  // dK += dS^T Q_i
-        mma_commit(empty(iq % R));            // Q_i (and its L, D) is done
+        accum(kTmDK, kTmDP, item_slot(iq), ii > 0);  // dK += dS^T Q_i
+        mma_commit(empty(item_slot(iq)));            // Q_i (and its L, D) is done
         if (has_next) {
-          score(dVd, (ido + 2) % R, kTmDP);  // dP^T_{i+1}
+          score(dVd, item_slot(ido + 2), kTmDP);  // dP^T_{i+1}
           mma_commit(bar(5));
         }
         return true;
@@ -572,30 +582,31 @@ __global__ void __launch_bounds__(320, 1)
       // about 20 cycles per MMA).
       auto steady = [&](int ii) -> bool {
         const int iq = 2 * ii, ido = 2 * ii + 1;
-        const uint32_t pb = ii & 1, pq = ((iq + 2) / R) & 1, pd = ((ido + 2) / R) & 1;
+        const uint32_t pb = ii & 1, pq = item_phase(iq + 2), pd = item_phase(ido + 2);
+        const int sq = item_slot(iq + 2), sd = item_slot(ido + 2), sqi = item_slot(iq), sdi = item_slot(ido);
         {
           const bool a = mbar_try_wait(bar(2), pb);
-          const bool b = mbar_try_wait(full((iq + 2) % R), pq);
+          const bool b = mbar_try_wait(full(sq), pq);
           if (!(a && b)) {
-            if (!mbar_wait(bar(2), pb, abort_flag) || !mbar_wait(full((iq + 2) % R), pq, abort_flag)) return false;
+            if (!mbar_wait(bar(2), pb, abort_flag) || !mbar_wait(full(sq), pq, abort_flag)) return false;
           }
         }
         tc_fence_after();
-        accum(kTmDV, kTmS, ido % R, true);  // dV += P^T dO_i
-        mma_commit(empty(ido % R));         // dO_i is done
-        score(dKd, (iq + 2) % R, kTmS);     // S^T_{i+1}
+        accum(kTmDV, kTmS, sdi, true);  // dV += P^T dO_i
+        mma_commit(empty(sdi));         // dO_i is done
+        score(dKd, sq, kTmS);           // S^T_{i+1}
         mma_commit(bar(1));
         {
           const bool a = mbar_try_wait(bar(6), pb);
-          const bool b = mbar_try_wait(full((ido + 2) % R), pd);
+          const bool b = mbar_try_wait(full(sd), pd);
           if (!(a && b)) {
-            if (!mbar_wait(bar(6), pb, abort_flag) || !mbar_wait(full((ido + 2) % R), pd, abort_flag)) return false;
+            if (!mbar_wait(bar(6), pb, abort_flag) || !mbar_wait(full(sd), pd, abort_flag)) return false;
           }
         }
         tc_fence_after();
-        accum(kTmDK, kTmDP, iq % R, true);  // dK += dS^T Q_i
-        mma_commit(empty(iq % R));          // Q_i (and its L, D) is done
-        score(dVd, (ido + 2) % R, kTmDP);   // dP^T_{i+1}
+        accum(kTmDK, kTmDP, sqi, true);  // dK += dS^T Q_i
+        mma_commit(empty(sqi));          // Q_i (and its L, D) is done
+        score(dVd, sd, kTmDP);           // dP^T_{i+1}
         mma_commit(bar(5));
         return true;
       };
@@ -621,12 +632,12 @@ __global__ void __launch_bounds__(320, 1)
     bool ok = true;
     for (int ii = 0; ii < nq; ++ii) {
       const int i = i0 + ii;
-      const int s = (2 * ii) % R;  // slot of Q_i, which carries the side buffer
+      const int s = item_slot(2 * ii);  // slot of Q_i, which carries the side buffer
       const float* const Ls = reinterpret_cast<const float*>(sbase + C::kKVSideOff + s * C::kSideBytes) + h * 64;
       const float* const Ds = Ls + 128;
       // the Q_i item's TMA barrier covers the side buffer (L, D) read below;
       // S^T_i comes from its MMA commit (dP^T_i, from its own, is waited for later)
-      bool got = mbar_wait(full(s), ((2 * ii) / R) & 1, abort_flag) && mbar_wait(bar(1), ii & 1, abort_flag);
+      bool got = mbar_wait(full(s), item_phase(2 * ii), abort_flag) && mbar_wait(bar(1), ii & 1, abort_flag);
       got = __all_sync(0xffffffffu, got);
       if (!got) {
         ok = false;
