@@ -504,8 +504,18 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     return 0
 
 
+def bwd_algorithmic_bytes(w: synth.Workload) -> int:
+    """Compulsory HBM bytes of one fa_bwd: Q, K, V, O, dO and LSE read, dQ, dK, dV written,
+    and the fp32 L and D workspace written by the first kernel and read by the second."""
+    bhnd = w.B * w.H * w.Nq * w.d
+    rows = w.B * w.H * w.Nq
+    return 2 * (5 + 3) * bhnd + 4 * rows + 2 * 8 * rows
+
+
 def run_bwd(args, w: synth.Workload, local_rank: int):
-    """Backward-pass timing line (not the headline metric): one fa_bwd per step."""
+    """Backward-pass timing line (not the headline metric): one fa_bwd per step.
+    FLOPs are counted as 2.5x the forward's; the two kernels execute 3.5x (S and dP
+    are recomputed in each), reported as roofline.executed_tflops."""
     import torch
 
     import exact_attention_19_gb300 as fa
@@ -525,6 +535,12 @@ def run_bwd(args, w: synth.Workload, local_rank: int):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    algo_bytes = bwd_algorithmic_bytes(w)
+    in_bytes = 2 * (q.numel() + k.numel() + v.numel() + o.numel() + do.numel())
+    big_inputs = in_bytes > L2_BYTES
+    flush = None if big_inputs else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    l2_note = (f"inputs larger than L2 ({in_bytes / 1e6:.0f} MB > {L2_BYTES / 1e6:.0f} MB)" if big_inputs
+               else f"L2 flushed between timed steps ({2 * L2_BYTES / 1e6:.0f} MB write)")
 
     def step():
         fa.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
@@ -533,23 +549,57 @@ def run_bwd(args, w: synth.Workload, local_rank: int):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local_rank)
+    except Exception:
+        gpu_id = str(local_rank)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
     torch.cuda.synchronize()
+    wall0 = time.time()
+    if big_inputs:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        elapsed = e0.elapsed_time(e1)
+    else:
+        elapsed = 0.0
+        for _ in range(args.steps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            elapsed += e0.elapsed_time(e1)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    time.sleep(0.15)
+    sampler.stop()
+    clocks = sampler.summary(wall0, wall1)
     st, word = fa.fa_fwd_status(None, clear=True)
     if st != 0:
         raise RuntimeError(f"kernel reported a wait timeout (status {word:#x})")
-    ms = e0.elapsed_time(e1) / args.steps
+    ms = elapsed / args.steps
     flops = 2.5 * w.flops
     peaks, kind = load_peaks()
     value = flops / (ms * 1e-3) / 1e12
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_gbs = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    roofline = roofline_entry(flops, algo_bytes, value, algo_bytes / (ms * 1e-3) / 1e9, peak_tf, peak_gbs)
+    roofline.update({"traffic": None, "peak_kind": f"{roofline['peak_kind']}, {kind}", "kernel": "fa_bwd (dQ + dK/dV)",
+                     "algorithmic_bytes": algo_bytes, "executed_tflops": 1.4 * value,
+                     "executed_frac": 1.4 * value / peak_tf})
+    config = dict(config_of(w))
+    config["l2"] = l2_note
     print(json.dumps({"metric": "attention bwd TFLOP/s (2.5x forward FLOPs)", "value": value, "unit": UNIT,
                       "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-                      "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "config": config_of(w),
-                      "frac_of_peak": value / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+                      "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "config": config,
+                      "frac_of_peak": value / peak_tf, "roofline": roofline, "clocks": clocks,
                       "gpu_launches": 2 * args.steps}), flush=True)
     return 0
 

@@ -119,3 +119,11 @@ def test_e2e_entry_reports_the_faster_mode_and_both_figures():
     assert e["serial_value"] == 500.0 and e["h2d_bytes_per_step"] == 100 and e["d2h_bytes_per_step"] == 10
     e = bench.e2e_entry(50.0, 0.08, 88.0, 0.05, 100, 10, 5)
     assert e["mode"] == "serial" and e["value"] == 88.0 and e["pipelined_value"] == 50.0
+
+
+def test_bwd_algorithmic_bytes_counts_every_tensor_once():
+    # 4 x 32 x 8192 x 128: eight bf16 tensors of 268,435,456 bytes (Q, K, V, O, dO read; dQ, dK, dV
+    # written), LSE read (4 B per row), L and D written then read (16 B per row)
+    w = synth.WORKLOADS["long_8192_d128"]
+    rows = 4 * 32 * 8192
+    assert bench.bwd_algorithmic_bytes(w) == 8 * 268435456 + 4 * rows + 16 * rows
