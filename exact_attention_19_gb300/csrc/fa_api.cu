@@ -335,14 +335,27 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   const int rc = d == 64 ? launch_d<64, true>(causal, mq, mk, mv, p, grid, stream)
                          : launch_d<128, true>(causal, mq, mk, mv, p, grid, stream);
   if (rc != FA_OK) return rc;
+  // The merge is a programmatic dependent launch: its CTAs may be scheduled
+  // while the sliced kernel's last CTAs run, and wait in the kernel for its
+  // completion, so its launch latency overlaps the forward's tail.
   const long long cgrid = (p.rows + 7) / 8;
-  if (d == 64)
-    fa::fa_splitkv_combine_kernel<64><<<static_cast<unsigned>(cgrid), 256, 0, stream>>>(p.o_part, p.lse_part, o, lse,
-                                                                                         p.rows, eff);
-  else
-    fa::fa_splitkv_combine_kernel<128><<<static_cast<unsigned>(cgrid), 256, 0, stream>>>(p.o_part, p.lse_part, o,
-                                                                                          lse, p.rows, eff);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cgrid));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const float* o_part = p.o_part;
+  const float* lse_part = p.lse_part;
+  const long long rows = p.rows;
+  const cudaError_t e = d == 64
+                            ? cudaLaunchKernelEx(&cfg, fa::fa_splitkv_combine_kernel<64>, o_part, lse_part, o, lse, rows, eff)
+                            : cudaLaunchKernelEx(&cfg, fa::fa_splitkv_combine_kernel<128>, o_part, lse_part, o, lse, rows, eff);
+  return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? FA_OK : FA_ERR_LAUNCH;
 }
 
 // ---------------------------------------------------------------------------

@@ -119,6 +119,10 @@ __global__ void __launch_bounds__(320, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // split-KV: the merge kernel is launched as a programmatic dependent of this
+  // grid; let it be scheduled once every CTA of this grid has started (it
+  // waits for this grid's completion and memory before reading the partials)
+  if (SPLIT) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (threadIdx.x == 0) {
     mbar_init(bar(kBarQ + 0), 1);
@@ -611,6 +615,9 @@ __global__ void __launch_bounds__(256) fa_splitkv_combine_kernel(const float* __
                                                                  const float* __restrict__ lse_part, void* o,
                                                                  float* lse, long long rows, int n_splits) {
   constexpr int kPer = D / 32;  // elements per lane
+  // launched as a programmatic dependent of the sliced forward: wait until that
+  // grid has completed and its partial results are visible (a no-op otherwise)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
