@@ -65,7 +65,8 @@ struct BwdCfg {
   static constexpr uint32_t kKVSideOff = kKVRingOff + kRingKV * kTileBytes;
   static constexpr uint32_t kKVBarOff = kKVSideOff + kRingKV * kSideBytes;
   static constexpr uint32_t kBarBytes = 512;
-  static constexpr uint32_t kSmemQ = kQBarOff + kBarBytes + 1024;
+  static constexpr uint32_t kQPartOff = kQBarOff + kBarBytes;  // dQ kernel: half-row sums of D (2 x 128 fp32)
+  static constexpr uint32_t kSmemQ = kQPartOff + 1024 + 1024;
   static constexpr uint32_t kSmemKV = kKVBarOff + kBarBytes + 1024;
   static constexpr uint32_t kIdescScore = idesc_bf16(128, 128, false);  // 128 x 128 over d
   static constexpr uint32_t kIdescAcc = idesc_bf16(128, D, true);       // 128 x D over 128 rows
@@ -76,7 +77,8 @@ struct BwdCfg {
 // dQ kernel
 // ---------------------------------------------------------------------------
 // barriers: 0 q_full, 1 s_full, 2 dp_full, 3 s_free, 4 ds_full, 5 dq_full,
-// 6 drain, then ring full[kRingQ], empty[kRingQ]
+// 6 drain, 7..10 the D half-sum exchange (one per TMEM lane quarter), then
+// ring full[kRingQ], empty[kRingQ]
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -90,8 +92,8 @@ __global__ void __launch_bounds__(320, 1)
   uint8_t* const sbase = smem_raw + (base - raw_addr);
   const uint32_t bar0 = base + C::kQBarOff;
   auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  auto full = [&](int s) -> uint32_t { return bar(7 + s); };
-  auto empty = [&](int s) -> uint32_t { return bar(7 + R + s); };
+  auto full = [&](int s) -> uint32_t { return bar(11 + s); };
+  auto empty = [&](int s) -> uint32_t { return bar(11 + R + s); };
   auto slot_addr = [&](int s) -> uint32_t { return base + C::kQRingOff + s * C::kTileBytes; };
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::kQBarOff + 448);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + C::kQBarOff + 452);
@@ -105,6 +107,7 @@ __global__ void __launch_bounds__(320, 1)
     mbar_init(bar(4), 256);
     mbar_init(bar(5), 1);
     mbar_init(bar(6), 1);
+    for (int q = 0; q < 4; ++q) mbar_init(bar(7 + q), 64);
     for (int s = 0; s < R; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
@@ -276,22 +279,40 @@ __global__ void __launch_bounds__(320, 1)
     const bool valid = row < p.Nq;
     const size_t grow = static_cast<size_t>(bh) * p.Nq + row;
     // D = rowsum(dO * O) in fp32, L = LSE * log2(e); padding rows: P = 0.
-    // Both halves compute the whole row's D, in the same order (same value).
+    // Each half sums its own D/2 columns with every load issued up front (one
+    // memory round trip), then the two half sums meet in shared memory and
+    // both halves add them in the same order (same value in both).
     float dsum = 0.f, lse2 = POS_INF;
     if (valid) {
-      const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + grow * D);
-      const uint4* drow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + grow * D);
-#pragma unroll 4
-      for (int i = 0; i < D / 8; ++i) {
-        const uint4 a = orow[i], b = drow[i];
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+      const uint4* orow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.o) + grow * D + h * (D / 2));
+      const uint4* drow = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.dout) + grow * D + h * (D / 2));
+      uint4 oa[D / 16], da[D / 16];
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) {
+        oa[i] = orow[i];
+        da[i] = drow[i];
+      }
+      lse2 = p.lse[grow] * 1.4426950408889634074f;
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) {
+        const uint32_t aw[4] = {oa[i].x, oa[i].y, oa[i].z, oa[i].w}, bw[4] = {da[i].x, da[i].y, da[i].z, da[i].w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           dsum = fmaf(__uint_as_float(aw[t] << 16), __uint_as_float(bw[t] << 16), dsum);
           dsum = fmaf(__uint_as_float(aw[t] & 0xFFFF0000u), __uint_as_float(bw[t] & 0xFFFF0000u), dsum);
         }
       }
-      lse2 = p.lse[grow] * 1.4426950408889634074f;
+    }
+    {
+      float* const part = reinterpret_cast<float*>(sbase + C::kQPartOff);  // [half][row]
+      part[h * 128 + row_local] = dsum;
+      mbar_arrive(bar(7 + wq));
+      bool got = __all_sync(0xffffffffu, mbar_wait(bar(7 + wq), 0, abort_flag));
+      if (got) {
+        dsum = part[row_local] + part[128 + row_local];
+      } else {
+        report_wait_failure(abort_flag, 1u);
+      }
     }
     if (h == 0) {
       const size_t prow = static_cast<size_t>(bh) * p.Nq_pad + row;
