@@ -102,7 +102,10 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* l
  * own row sum, and L_s = log2 of that row sum in base-2 scaled-logit units.
  * A second kernel on the same stream merges the slices by the rule under which
  * the online-softmax state (m, l, O) is insensitive to block order ("llm-infra-
- * atlas / FlashAttention 01", section 2):
+ * atlas / FlashAttention 01", section 2).  It is launched as a programmatic
+ * dependent of the first (it may be scheduled while the first one's last CTAs
+ * run and waits on the device for its completion), so stream order and the
+ * results are those of two plain launches:
  *   L = log2 sum_s 2^L_s,   O = sum_s 2^(L_s - L) O_s,   LSE = L * ln 2.
  *
  * Arguments as in fa_fwd, plus:
