@@ -69,6 +69,44 @@ def read_traffic(workload: str, src_hash: str):
     return None
 
 
+def timed_steps(torch, step, steps, stream, flush):
+    """Device time of `steps` calls of step(), with an event on the launching stream at every step
+    boundary.  Inputs larger than L2 run back to back; otherwise the L2 is flushed before each
+    step, outside its events.  Returns (total ms, per-step ms)."""
+    if flush is None:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+        ev[0].record(stream)
+        for i in range(steps):
+            step()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        return ev[0].elapsed_time(ev[steps]), [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    total, per = 0.0, []
+    for _ in range(steps):
+        flush.fill_(1.0)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1)
+        per.append(t)
+        total += t
+    return total, per
+
+
+def step_stats(per_step_ms):
+    """Median and 10th / 90th percentiles of the per-step device times (ms)."""
+    xs = sorted(per_step_ms)
+    if not xs:
+        return None
+
+    def pct(q):
+        return xs[min(len(xs) - 1, max(0, int(round(q * (len(xs) - 1)))))]
+
+    return {"median": pct(0.5), "p10": pct(0.1), "p90": pct(0.9)}
+
+
 def roofline_entry(flops, algo_bytes, achieved_tflops, achieved_gbs, peak_tflops, peak_gbs):
     """The binding roofline of a workload: the tensor pipe when its intensity
     (FLOPs per compulsory byte) is at or above the ridge peak_tflops / peak_gbs,
@@ -344,24 +382,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     barrier()
     torch.cuda.synchronize()
     wall0 = time.time()
-    if big_inputs:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        elapsed = e0.elapsed_time(e1)
-    else:
-        elapsed = 0.0
-        for _ in range(args.steps):
-            flush.fill_(1.0)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            step()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            elapsed += e0.elapsed_time(e1)
+    elapsed, per_step = timed_steps(torch, step, args.steps, stream, flush)
     barrier()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -499,6 +520,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
                          int(2 * o.numel() + 4 * lse.numel()), e2e_steps),
         "gpu_launches": args.steps * launches_per_step, "clocks": clocks,
         "pct_of_peak": 100.0 * achieved / peak,  # of the dense bf16 peak, whatever the binding roofline
+        "ms_step_stats": step_stats(per_step), "peak_mem_bytes": int(torch.cuda.max_memory_allocated(dev)),
     }
     print(json.dumps(line), flush=True)
     return 0
@@ -558,24 +580,7 @@ def run_bwd(args, w: synth.Workload, local_rank: int):
     time.sleep(0.3)
     torch.cuda.synchronize()
     wall0 = time.time()
-    if big_inputs:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        elapsed = e0.elapsed_time(e1)
-    else:
-        elapsed = 0.0
-        for _ in range(args.steps):
-            flush.fill_(1.0)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            step()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            elapsed += e0.elapsed_time(e1)
+    elapsed, per_step = timed_steps(torch, step, args.steps, stream, flush)
     torch.cuda.synchronize()
     wall1 = time.time()
     time.sleep(0.15)
@@ -600,6 +605,7 @@ def run_bwd(args, w: synth.Workload, local_rank: int):
                       "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
                       "higher_is_better": True, "dtype": "bf16", "data": "synthetic", "config": config,
                       "frac_of_peak": value / peak_tf, "roofline": roofline, "clocks": clocks,
+                      "ms_step_stats": step_stats(per_step), "peak_mem_bytes": int(torch.cuda.max_memory_allocated(dev)),
                       "gpu_launches": 2 * args.steps}), flush=True)
     return 0
 

@@ -127,3 +127,38 @@ def test_bwd_algorithmic_bytes_counts_every_tensor_once():
     w = synth.WORKLOADS["long_8192_d128"]
     rows = 4 * 32 * 8192
     assert bench.bwd_algorithmic_bytes(w) == 8 * 268435456 + 4 * rows + 16 * rows
+
+
+def test_step_stats_percentiles():
+    st = bench.step_stats([5.0, 1.0, 3.0, 2.0, 4.0])
+    assert st == {"median": 3.0, "p10": 1.0, "p90": 5.0}
+    assert bench.step_stats([]) is None
+
+
+def test_timed_steps_without_flush_on_cpu_events():
+    # the function's contract on a fake torch: one event per step boundary, totals add up
+    class Ev:
+        t = 0.0
+
+        def __init__(self, enable_timing=True):
+            self.stamp = None
+
+        def record(self, stream=None):
+            Ev.t += 1.0
+            self.stamp = Ev.t
+
+        def elapsed_time(self, other):
+            return other.stamp - self.stamp
+
+    class FakeCuda:
+        Event = Ev
+
+        @staticmethod
+        def synchronize():
+            pass
+
+    class FakeTorch:
+        cuda = FakeCuda
+
+    total, per = bench.timed_steps(FakeTorch, lambda: None, 4, None, None)
+    assert per == [1.0, 1.0, 1.0, 1.0] and total == 4.0
