@@ -43,6 +43,7 @@ KERNEL_SOURCES = ["exact_attention_19_gb300/csrc/fa_fwd_kernel.cuh", "exact_atte
                   "exact_attention_19_gb300/csrc/fa_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_kernel_dram_traffic.md")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+NOMINAL_BF16_TFLOPS = 2250.0  # nominal dense bf16 tensor peak of one GB300 (not measured; context only)
 
 
 # ----------------------------------------------------------------------------
@@ -489,6 +490,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     roofline = roofline_entry(w.flops, w.algorithmic_bytes, achieved, achieved_gbs, peak, hbm)
     roofline.update({"traffic": traffic, "peak_kind": f"{roofline['peak_kind']}, {peaks_kind}",
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
+                     "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
                      "kernel": KERNEL_NAME, "kernel_source": src_hash,
                      "algorithmic_bytes": w.algorithmic_bytes})
 
