@@ -48,10 +48,10 @@ int g_dev_sms_or(int dev, int fallback) {
 }
 std::mutex g_dev_mutex;
 
-template <int D, int MASK, bool SPLIT>
+template <int D, int MASK, bool SPLIT, int TILES = 2>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, MASK, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(fa::Cfg<D>::kSmemBytes));
+  return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, MASK, SPLIT, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fa::Cfg<D, TILES>::kSmemBytes));
 }
 
 template <int D>
@@ -69,11 +69,13 @@ bool set_bwd_smem_attrs() {
 
 template <int D>
 bool set_smem_attrs() {
-  return set_smem_attr<D, fa::kMaskNone, false>() == cudaSuccess &&
-         set_smem_attr<D, fa::kMaskCausal, false>() == cudaSuccess &&
-         set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
-         set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
-         set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
+  bool ok = set_smem_attr<D, fa::kMaskNone, false>() == cudaSuccess &&
+            set_smem_attr<D, fa::kMaskCausal, false>() == cudaSuccess &&
+            set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
+            set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
+            set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
+  if constexpr (D == 64) ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess;
+  return ok;
 }
 
 int prepare_device(int dev) {
@@ -130,13 +132,20 @@ bool make_map(CUtensorMap* map, const void* ptr, int D, long long N, long long B
   return r == CUDA_SUCCESS;
 }
 
-template <int D, int MASK, bool SPLIT>
+template <int D, int MASK, bool SPLIT, int TILES = 2>
 int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
            long long grid, cudaStream_t stream) {
-  fa::fa_fwd_kernel<D, MASK, SPLIT><<<static_cast<unsigned>(grid), fa::Cfg<D>::kThreads,
-                                      fa::Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, p);
+  using C = fa::Cfg<D, TILES>;
+  fa::fa_fwd_kernel<D, MASK, SPLIT, TILES><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
+      mq, mk, mv, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
+
+// Single query tile per CTA (two CTAs per SM) for causal attention at d = 64
+// over at most this many keys: there the fixed per-CTA cost weighs most
+// (8 x 12 x 1024: +5.5%, 2 x 4 x 2048: +8%; 4 x 32 x 8192: -10%, so longer
+// key ranges keep two tiles per CTA).
+constexpr int kSingleTileMaxKeys = 2048;
 
 // no mask or the causal mask (split or not)
 template <int D, bool SPLIT>
@@ -258,6 +267,12 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   bool noop = false;
   const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &p, &dev, &noop);
   if (st != FA_OK || noop) return st;
+  if (d == 64 && causal && Nk <= kSingleTileMaxKeys) {
+    p.n_pairs = (Nq + 127) / 128;  // one query tile per CTA
+    const long long grid = static_cast<long long>(B) * H * p.n_pairs;
+    if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
+    return launch<64, fa::kMaskCausal, false, 1>(mq, mk, mv, p, grid, stream);
+  }
   const long long grid = static_cast<long long>(B) * H * p.n_pairs;
   return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, p, grid, stream)
                  : launch_d<128, false>(causal, mq, mk, mv, p, grid, stream);

@@ -44,7 +44,7 @@ struct FwdParams {
   void* o;            // bf16 [BH, Nq, D]
   float* lse;         // fp32 [BH, Nq]
   int Nq, Nk;
-  int n_pairs;        // ceil(Nq / 256): query-tile pairs per (b, h)
+  int n_pairs;        // CTAs per (b, h): ceil(Nq / (128 * TILES)), query-tile pairs or single tiles
   float scale_log2;   // scale * log2(e)
   // window mask only: key j is visible to query row i iff
   //   i + diag_off - win_left <= j <= i + diag_off + win_right  (a negative bound: unbounded)
@@ -58,26 +58,36 @@ struct FwdParams {
   long long rows;     // BH * Nq
 };
 
-template <int D>
+// TILES = 2: two query tiles per CTA (softmax ping-pong), one CTA per SM.
+// TILES = 1 (d = 64): one query tile per CTA in half the TMEM and shared
+// memory, so that two CTAs share an SM and each one's MMA checks, start and
+// end overlap the other's work; taken for short causal key ranges, where the
+// fixed per-CTA cost weighs most.
+template <int D, int TILES = 2>
 struct Cfg {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kThreads = 320;
+  static_assert(TILES == 2 || (TILES == 1 && D == 64), "query tiles per CTA");
+  static constexpr int kTiles = TILES;
+  static constexpr int kWarpProd = 4 * kTiles, kWarpMma = 4 * kTiles + 1;
+  static constexpr int kThreads = 32 * (4 * kTiles + 2);
+  static constexpr int kMinBlocks = (kTiles == 1) ? 2 : 1;  // CTAs per SM
   static constexpr int kBM = 128;  // query rows per tile (MMA M)
   static constexpr int kBN = 128;  // keys per tile
-  static constexpr int kRing = (D == 128) ? 5 : 8;  // K/V ring slots (K and V alternate)
+  static constexpr int kRing = (D == 128 || kTiles == 1) ? 5 : 8;  // K/V ring slots (K and V alternate)
   static constexpr int kBoxes = D / 64;  // 128-byte swizzle boxes per row
   static constexpr uint32_t kBoxBytes = 128u * 128u;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
   static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kRingOff = 2 * kTileBytes;
+  static constexpr uint32_t kRingOff = kTiles * kTileBytes;
   static constexpr uint32_t kBarOff = kRingOff + kRing * kTileBytes;
   static constexpr uint32_t kBarBytes = 512;
   static constexpr uint32_t kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = 256, kTmO1 = 256 + D;
+  static constexpr uint32_t kTmemCols = (kTiles == 1) ? 256 : 512;
+  static constexpr uint32_t kTmS0 = 0, kTmS1 = 128, kTmO0 = (kTiles == 1) ? 128 : 256, kTmO1 = 256 + D;
   static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);  // S = Q K^T
   static constexpr uint32_t kIdescO = idesc_bf16(128, D, true);     // O += P V
   static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kMinBlocks == 1 || kMinBlocks * (kSmemBytes + 1024) <= 233472, "two CTAs per SM");
 };
 
 // barrier slots (8 bytes each) inside the barrier block; the ring's full
@@ -99,11 +109,11 @@ __device__ __forceinline__ void report_wait_failure(volatile int* abort, unsigne
 // of its pair and writes a partial result; fa_splitkv_combine_kernel merges them.
 enum : int { kMaskNone = 0, kMaskCausal = 1, kMaskWindow = 2 };
 
-template <int D, int MASK, bool SPLIT>
-__global__ void __launch_bounds__(320, 1)
+template <int D, int MASK, bool SPLIT, int TILES = 2>
+__global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBlocks)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, TILES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -141,7 +151,7 @@ __global__ void __launch_bounds__(320, 1)
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 9) {
+  if (warp == C::kWarpMma) {
     tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -160,7 +170,8 @@ __global__ void __launch_bounds__(320, 1)
   int bh = cta / p.n_pairs;
   int pair = cta % p.n_pairs;
   if (MASK == kMaskCausal) {
-    // Causal pairs differ in work (pair i sees 2i + 2 K/V tiles).  Heads are
+    // Causal CTAs differ in work (pair i sees 2i + 2 K/V tiles, a single
+    // tile i sees i + 1).  Heads are
     // taken in groups whose K/V fit in a quarter of the L2; inside a group the
     // heaviest pairs of all its heads run first, so a group's last wave holds
     // its lightest pairs (longest-processing-time-first order), while the
@@ -180,10 +191,10 @@ __global__ void __launch_bounds__(320, 1)
   int row0[2], jlo[2], jhi[2], nkv[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    const int qt = 2 * pair + t;
+    const int qt = C::kTiles * pair + t;
     row0[t] = qt * C::kBM;
     int lo = 0, hi = 0;
-    if (row0[t] < p.Nq) {
+    if (t < C::kTiles && row0[t] < p.Nq) {
       hi = n_kv_all;
       if (MASK == kMaskCausal) {
         hi = min(n_kv_all, qt + 1);
@@ -216,7 +227,7 @@ __global__ void __launch_bounds__(320, 1)
   }
   const int n_items = 2 * n_max;  // ring items: K_j = item 2j, V_j = item 2j+1
 
-  if (warp == 8) {
+  if (warp == C::kWarpProd) {
     // ======================= TMA producer =================================
     if (lane == 0) {
       tma_prefetch_map(&tmQ);
@@ -252,7 +263,7 @@ __global__ void __launch_bounds__(320, 1)
           if (nkv[t] > 0) mbar_wait(bar(kBarQ + t), 0, nullptr);
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == C::kWarpMma) {
     // ======================= MMA issuer ====================================
     if (lane == 0) {
       // descriptors: start address lives in bits 0-13 (address >> 4), so a
@@ -598,7 +609,7 @@ __global__ void __launch_bounds__(320, 1)
   // ---- teardown -----------------------------------------------------------
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::kWarpMma) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);

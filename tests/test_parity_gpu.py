@@ -68,6 +68,13 @@ def test_ragged_square(n, d, causal, n_splits):
     _check_full(synth.Workload(f"ragged{n}", 1, 2, n, n, d, causal, seed=500 + n), n_splits)
 
 
+# causal attention at d = 64 over at most 2048 keys runs one query tile per CTA
+# (two CTAs per SM), longer key ranges two: both sides of the switch, every element
+@pytest.mark.parametrize("n", [2047, 2048, 2049])
+def test_causal_d64_tile_count_switch(n):
+    _check_full(synth.Workload(f"switch{n}", 2, 3, n, n, 64, True, seed=900 + n), 1)
+
+
 @pytest.mark.parametrize("n_splits", [None, 1])
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("nq,nk", [(100, 300), (513, 64), (1, 1000), (256, 129), (700, 4097)])
