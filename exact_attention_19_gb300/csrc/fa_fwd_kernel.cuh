@@ -27,6 +27,10 @@
 // Shared memory: Q0, Q1, then the K/V ring; each tile is 128 rows x D bf16
 // stored as D/64 boxes of 128 rows x 128 bytes with the 128-byte swizzle that
 // TMA writes and the MMA descriptors read (K-major for Q and K, MN-major for V).
+// The single-tile instantiation (TILES = 1, d = 64, short causal key ranges)
+// keeps warps 0-3 for its one query tile, warp 4 as producer and warp 5 as MMA
+// issuer, 256 TMEM columns (S [0,128), O [128,192)) and a 5-slot ring, so two
+// CTAs share an SM.
 #pragma once
 
 #include <cstdint>
