@@ -124,6 +124,15 @@ def test_multi_batch_head(d):
     _check_full(synth.Workload("bh", 2, 7, 130, 390, d, False, seed=32))
 
 
+# thousands of short heads: grids of several thousand small CTAs (single-tile CTAs
+# for the causal d = 64 case), causal scheduling groups far smaller than B * H,
+# and a ragged second query tile of two rows in every head
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_short_heads(d, causal):
+    _check_full(synth.Workload("many", 16, 128, 130, 130, d, causal, seed=40 + d + causal), 1)
+
+
 # --- degenerate and numerically hard cases -----------------------------------
 @pytest.mark.parametrize("d", [64, 128])
 def test_single_key(d):
