@@ -81,6 +81,15 @@ def test_bwd_multi_head_and_wide_logits():
     _check(synth.Workload("bwd_bh", 3, 2, 200, 200, 64, False, sigma_q=3.0, seed=821))
 
 
+# hundreds of short heads with a ragged second tile: grids of ~1000 small CTAs in
+# both backward kernels (and the single-tile forward for causal d = 64)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_many_short_heads(d, causal):
+    _check(synth.Workload("bwd_many", 8, 64, 130, 130, d, causal, seed=840 + d + causal),
+           f"many heads d={d} causal={causal}")
+
+
 def test_bwd_deterministic():
     w = synth.Workload("bwd_det", 1, 3, 700, 700, 128, True, seed=830)
     q, k, v = w.make()
