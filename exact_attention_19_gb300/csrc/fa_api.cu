@@ -133,11 +133,12 @@ bool make_map(CUtensorMap* map, const void* ptr, int D, long long N, long long B
 }
 
 template <int D, int MASK, bool SPLIT, int TILES = 2>
-int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
+int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
+           const fa::FwdParams& p,
            long long grid, cudaStream_t stream) {
   using C = fa::Cfg<D, TILES>;
   fa::fa_fwd_kernel<D, MASK, SPLIT, TILES><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
-      mq, mk, mv, p);
+      mq, mk, mv, mo, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -150,9 +151,9 @@ constexpr int kSingleTileMaxKeys = 2048;
 // no mask or the causal mask (split or not)
 template <int D, bool SPLIT>
 int launch_d(bool causal, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-             const fa::FwdParams& p, long long grid, cudaStream_t stream) {
-  return causal ? launch<D, fa::kMaskCausal, SPLIT>(mq, mk, mv, p, grid, stream)
-                : launch<D, fa::kMaskNone, SPLIT>(mq, mk, mv, p, grid, stream);
+             const CUtensorMap& mo, const fa::FwdParams& p, long long grid, cudaStream_t stream) {
+  return causal ? launch<D, fa::kMaskCausal, SPLIT>(mq, mk, mv, mo, p, grid, stream)
+                : launch<D, fa::kMaskNone, SPLIT>(mq, mk, mv, mo, p, grid, stream);
 }
 
 template <int D, bool CAUSAL>
@@ -171,7 +172,7 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
 // maps and the common parameters; *noop is set when Nq == 0.
 int prepare_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
                  int d, float scale, int causal, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
-                 fa::FwdParams* p, int* dev_out, bool* noop) {
+                 CUtensorMap* mo, fa::FwdParams* p, int* dev_out, bool* noop) {
   *noop = false;
   // With Nq == 0 nothing is read or written, so the (empty) tensors may be NULL.
   if ((Nq != 0 && (!q || !o || !lse)) || !k || !v) return FA_ERR_NULL;
@@ -200,7 +201,8 @@ int prepare_call(const void* q, const void* k, const void* v, void* o, float* ls
   if (!is_device_pointer(q, dev) || !is_device_pointer(k, dev) || !is_device_pointer(v, dev) ||
       !is_device_pointer(o, dev) || !is_device_pointer(lse, dev))
     return FA_ERR_POINTER;
-  if (!make_map(mq, q, d, Nq, BH) || !make_map(mk, k, d, Nk, BH) || !make_map(mv, v, d, Nk, BH))
+  if (!make_map(mq, q, d, Nq, BH) || !make_map(mk, k, d, Nk, BH) || !make_map(mv, v, d, Nk, BH) ||
+      !make_map(mo, o, d, Nq, BH))
     return FA_ERR_LAUNCH;
   p->o = o;
   p->lse = lse;
@@ -261,41 +263,41 @@ const char* fa_strerror(int status) {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
            int d, float scale, int causal, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   fa::FwdParams p;
   int dev = -1;
   bool noop = false;
-  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &p, &dev, &noop);
+  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &mo, &p, &dev, &noop);
   if (st != FA_OK || noop) return st;
   if (d == 64 && causal && Nk <= kSingleTileMaxKeys) {
     p.n_pairs = (Nq + 127) / 128;  // one query tile per CTA
     const long long grid = static_cast<long long>(B) * H * p.n_pairs;
     if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
-    return launch<64, fa::kMaskCausal, false, 1>(mq, mk, mv, p, grid, stream);
+    return launch<64, fa::kMaskCausal, false, 1>(mq, mk, mv, mo, p, grid, stream);
   }
   const long long grid = static_cast<long long>(B) * H * p.n_pairs;
-  return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, p, grid, stream)
-                 : launch_d<128, false>(causal, mq, mk, mv, p, grid, stream);
+  return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, mo, p, grid, stream)
+                 : launch_d<128, false>(causal, mq, mk, mv, mo, p, grid, stream);
 }
 
 int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                   int Nk, int d, float scale, int window_left, int window_right, cudaStream_t stream) {
   if (window_left < -1 || window_right < -1) return FA_ERR_SHAPE;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   fa::FwdParams p;
   int dev = -1;
   bool noop = false;
-  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, 0, &mq, &mk, &mv, &p, &dev, &noop);
+  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, 0, &mq, &mk, &mv, &mo, &p, &dev, &noop);
   if (st != FA_OK || noop) return st;
   p.win_left = window_left;
   p.win_right = window_right;
   p.diag_off = Nk - Nq;  // bottom-right: the window's diagonal ends at (Nq - 1, Nk - 1)
   const long long grid = static_cast<long long>(B) * H * p.n_pairs;
   if (window_left < 0 && window_right < 0)  // no bound on either side: no mask
-    return d == 64 ? launch<64, fa::kMaskNone, false>(mq, mk, mv, p, grid, stream)
-                   : launch<128, fa::kMaskNone, false>(mq, mk, mv, p, grid, stream);
-  return d == 64 ? launch<64, fa::kMaskWindow, false>(mq, mk, mv, p, grid, stream)
-                 : launch<128, fa::kMaskWindow, false>(mq, mk, mv, p, grid, stream);
+    return d == 64 ? launch<64, fa::kMaskNone, false>(mq, mk, mv, mo, p, grid, stream)
+                   : launch<128, fa::kMaskNone, false>(mq, mk, mv, mo, p, grid, stream);
+  return d == 64 ? launch<64, fa::kMaskWindow, false>(mq, mk, mv, mo, p, grid, stream)
+                 : launch<128, fa::kMaskWindow, false>(mq, mk, mv, mo, p, grid, stream);
 }
 
 size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int Nk, int d, int n_splits) {
@@ -327,11 +329,11 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    int d, float scale, int causal, int n_splits, void* workspace, size_t workspace_bytes,
                    cudaStream_t stream) {
   if (n_splits < 1 || n_splits > 64) return FA_ERR_SHAPE;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   fa::FwdParams p;
   int dev = -1;
   bool noop = false;
-  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &p, &dev, &noop);
+  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &mo, &p, &dev, &noop);
   if (st != FA_OK || noop) return st;
   int tiles = 0, eff = 0;
   split_shape(Nk, n_splits, &tiles, &eff);
@@ -347,8 +349,8 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   p.lse_part = p.o_part + static_cast<size_t>(eff) * p.rows * d;
   const long long grid = static_cast<long long>(B) * H * p.n_pairs * eff;
   if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
-  const int rc = d == 64 ? launch_d<64, true>(causal, mq, mk, mv, p, grid, stream)
-                         : launch_d<128, true>(causal, mq, mk, mv, p, grid, stream);
+  const int rc = d == 64 ? launch_d<64, true>(causal, mq, mk, mv, mo, p, grid, stream)
+                         : launch_d<128, true>(causal, mq, mk, mv, mo, p, grid, stream);
   if (rc != FA_OK) return rc;
   // The merge is a programmatic dependent launch: its CTAs may be scheduled
   // while the sliced kernel's last CTAs run, and wait in the kernel for its

@@ -27,6 +27,9 @@
 // Shared memory: Q0, Q1, then the K/V ring; each tile is 128 rows x D bf16
 // stored as D/64 boxes of 128 rows x 128 bytes with the 128-byte swizzle that
 // TMA writes and the MMA descriptors read (K-major for Q and K, MN-major for V).
+// Epilogue: once a query tile's last MMA has completed its Q buffer is free;
+// its warps write O / l there as bf16 in the same swizzled box layout and one
+// thread stores the tile with TMA (rows past Nq are clipped by the tensor map).
 // The single-tile instantiation (TILES = 1, d = 64, short causal key ranges)
 // keeps warps 0-3 for its one query tile, warp 4 as producer and warp 5 as MMA
 // issuer, 256 TMEM columns (S [0,128), O [128,192)) and a 5-slot ring, so two
@@ -96,7 +99,7 @@ struct Cfg {
 
 // barrier slots (8 bytes each) inside the barrier block; the ring's full
 // barriers start at kBarRing, its empty barriers right after them
-enum : int { kBarQ = 0, kBarS = 2, kBarP = 4, kBarO = 6, kBarDrain = 8, kBarRing = 9 };
+enum : int { kBarQ = 0, kBarS = 2, kBarP = 4, kBarO = 6, kBarDrain = 8, kBarEpi = 9, kBarRing = 11 };
 constexpr uint32_t kTmemSlotOff = 448, kAbortOff = 452;
 
 __device__ __forceinline__ void report_wait_failure(volatile int* abort, unsigned role) {
@@ -116,7 +119,8 @@ enum : int { kMaskNone = 0, kMaskCausal = 1, kMaskWindow = 2 };
 template <int D, int MASK, bool SPLIT, int TILES = 2>
 __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBlocks)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const FwdParams p) {
   using C = Cfg<D, TILES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -148,6 +152,8 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
     mbar_init(bar(kBarO + 0), 1);
     mbar_init(bar(kBarO + 1), 1);
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarEpi + 0), 128);
+    mbar_init(bar(kBarEpi + 1), 128);
     for (int s = 0; s < C::kRing; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
@@ -237,6 +243,7 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmO);
       for (int t = 0; t < 2; ++t) {
         if (nkv[t] == 0) continue;
         const uint32_t dst = base + C::kQOff + t * C::kTileBytes;
@@ -553,7 +560,15 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
         const bool store = row < p.Nq;
         const size_t grow = static_cast<size_t>(bh) * p.Nq + row;  // row within [BH * Nq]
         if (!SPLIT) {
-          uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + grow * D);
+          // O / l in bf16 is staged in this tile's Q buffer (no MMA reads it
+          // once the tile's O barrier has flipped), laid out as the 128-byte
+          // swizzled boxes the O tensor map describes: 16-byte chunk c of row
+          // r of a box sits at r * 128 + ((c ^ (r & 7)) * 16), so a warp's 32
+          // rows cover every bank once per 8 rows.  One thread then writes the
+          // tile with TMA stores, which drop the rows past Nq.
+          const uint32_t stage = base + C::kQOff + static_cast<uint32_t>(t) * C::kTileBytes +
+                                 static_cast<uint32_t>(row_local) * 128u;
+          const uint32_t swz = static_cast<uint32_t>(row_local & 7);
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t o[32];
@@ -563,15 +578,29 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
 #pragma unroll
             for (int i = 0; i < 16; ++i)
               w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-            if (store) {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                orow[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + i);  // 16-byte chunk within the box
+              st_shared_v4(stage + static_cast<uint32_t>(cc >> 1) * C::kBoxBytes + ((chunk ^ swz) << 4), w[4 * i],
+                           w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
             }
           }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kBarEpi + t));
           if (store) {
             const float lse = (l > 0.f) ? (m_bar + __log2f(l)) * 0.69314718055994530942f : NEG_INF;
             p.lse[grow] = lse;
+          }
+          if (row_local == 0) {
+            if (mbar_wait(bar(kBarEpi + t), 0, abort_flag)) {
+              const uint32_t src = base + C::kQOff + static_cast<uint32_t>(t) * C::kTileBytes;
+#pragma unroll
+              for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(&tmO, src + b * C::kBoxBytes, b * 64, row0[t], bh);
+              bulk_commit_group();
+              bulk_wait_group_read0();
+            } else {
+              report_wait_failure(abort_flag, 8u);
+            }
           }
         } else {
           // partial: O / l in fp32 and the base-2 log-sum-exp of this slice
