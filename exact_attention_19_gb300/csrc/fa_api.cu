@@ -158,13 +158,14 @@ int launch_d(bool causal, const CUtensorMap& mq, const CUtensorMap& mk, const CU
 
 template <int D, bool CAUSAL>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
-               const fa::BwdParams& p, long long bh, cudaStream_t stream) {
+               const CUtensorMap& mdq, const CUtensorMap& mdk, const CUtensorMap& mdv, const fa::BwdParams& p,
+               long long bh, cudaStream_t stream) {
   using C = fa::BwdCfg<D>;
   fa::fa_bwd_dq_kernel<D, CAUSAL><<<static_cast<unsigned>(bh * p.n_qt), C::kThreads, C::kSmemQ, stream>>>(
-      mq, mk, mv, mdo, p);
+      mq, mk, mv, mdo, mdq, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   fa::fa_bwd_dkdv_kernel<D, CAUSAL><<<static_cast<unsigned>(bh * p.n_kt), C::kThreads, C::kSmemKV, stream>>>(
-      mq, mk, mv, mdo, p);
+      mq, mk, mv, mdo, mdk, mdv, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
@@ -455,9 +456,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   if (prep != FA_OK) return prep;
   for (const void* x : ptrs)
     if (!is_device_pointer(x, dev)) return FA_ERR_POINTER;
-  CUtensorMap mq, mk, mv, mdo;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
   if (!make_map(&mq, q, d, Nq, BH) || !make_map(&mk, k, d, Nk, BH) || !make_map(&mv, v, d, Nk, BH) ||
-      !make_map(&mdo, dout, d, Nq, BH))
+      !make_map(&mdo, dout, d, Nq, BH) || !make_map(&mdq, dq, d, Nq, BH) || !make_map(&mdk, dk, d, Nk, BH) ||
+      !make_map(&mdv, dv, d, Nk, BH))
     return FA_ERR_LAUNCH;
   fa::BwdParams p;
   p.o = o;
@@ -476,10 +478,10 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   if (d == 64)
-    return causal ? launch_bwd<64, true>(mq, mk, mv, mdo, p, BH, stream)
-                  : launch_bwd<64, false>(mq, mk, mv, mdo, p, BH, stream);
-  return causal ? launch_bwd<128, true>(mq, mk, mv, mdo, p, BH, stream)
-                : launch_bwd<128, false>(mq, mk, mv, mdo, p, BH, stream);
+    return causal ? launch_bwd<64, true>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream)
+                  : launch_bwd<64, false>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream);
+  return causal ? launch_bwd<128, true>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream)
+                : launch_bwd<128, false>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream);
 }
 
 int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear) {

@@ -78,12 +78,12 @@ struct BwdCfg {
 // ---------------------------------------------------------------------------
 // barriers: 0 q_full, 1 s_full, 2 dp_full, 3 s_free, 4 ds_full, 5 dq_full,
 // 6 drain, 7..10 the D half-sum exchange (one per TMEM lane quarter), then
-// ring full[kRingQ], empty[kRingQ]
+// ring full[kRingQ], empty[kRingQ], then the epilogue's staging barrier
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                     const BwdParams p) {
+                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingQ;
   extern __shared__ uint8_t smem_raw[];
@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
+    mbar_init(bar(11 + 2 * R), 256);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -142,6 +143,7 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmDO);
+      tma_prefetch_map(&tmDQ);
       mbar_arrive_expect_tx(bar(0), 2 * C::kTileBytes);
       for (int b = 0; b < C::kBoxes; ++b) {
         tma_load_3d(base + b * C::kBoxBytes, &tmQ, bar(0), b * 64, row0, bh);
@@ -390,7 +392,11 @@ __global__ void __launch_bounds__(320, 1)
         report_wait_failure(abort_flag, 8u);
       } else {
         tc_fence_after();
-        uint4* const out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * D + h * (D / 2));
+        // dQ in bf16 is staged in the Q buffer (free once dq_full has flipped)
+        // in the 128-byte swizzled box layout of the dQ tensor map, then one
+        // thread stores the tile with TMA (rows past Nq are dropped)
+        const uint32_t stage = base + static_cast<uint32_t>(row_local) * 128u;
+        const uint32_t swz = static_cast<uint32_t>(row_local & 7);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
           uint32_t o[32];
@@ -400,9 +406,24 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             w[i] = pack_bf16(__uint_as_float(o[2 * i]) * p.scale, __uint_as_float(o[2 * i + 1]) * p.scale);
-          if (valid) {
+          const int col = h * (D / 2) + cc * 32;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) out[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t chunk = static_cast<uint32_t>(((col & 63) >> 3) + i);
+            st_shared_v4(stage + static_cast<uint32_t>(col >> 6) * C::kBoxBytes + ((chunk ^ swz) << 4), w[4 * i],
+                         w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(11 + 2 * R));
+        if (threadIdx.x == 0) {
+          if (mbar_wait(bar(11 + 2 * R), 0, abort_flag)) {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(&tmDQ, base + b * C::kBoxBytes, b * 64, row0, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();
+          } else {
+            report_wait_failure(abort_flag, 8u);
           }
         }
       }
@@ -422,11 +443,12 @@ __global__ void __launch_bounds__(320, 1)
 // ---------------------------------------------------------------------------
 // barriers: 0 kv_full, 1 s_full (S^T), 2 p_done (P^T written), 3 acc_full,
 // 4 drain, 5 dp_full (dP^T), 6 ds_done (dS^T written), then ring
-// full[kRingKV], empty[kRingKV]
+// full[kRingKV], empty[kRingKV], then the epilogue's staging barrier
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV,
                        const BwdParams p) {
   using C = BwdCfg<D>;
   constexpr int R = C::kRingKV;
@@ -465,6 +487,7 @@ __global__ void __launch_bounds__(320, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
+    mbar_init(bar(7 + 2 * R), 256);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -493,6 +516,8 @@ __global__ void __launch_bounds__(320, 1)
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmDO);
+      tma_prefetch_map(&tmDK);
+      tma_prefetch_map(&tmDV);
       mbar_arrive_expect_tx(bar(0), 2 * C::kTileBytes);
       for (int b = 0; b < C::kBoxes; ++b) {
         tma_load_3d(base + b * C::kBoxBytes, &tmK, bar(0), b * 64, key0, bh);
@@ -734,30 +759,51 @@ __global__ void __launch_bounds__(320, 1)
         report_wait_failure(abort_flag, 8u);
       } else {
         tc_fence_after();
-        const bool store = key < p.Nk;
-        const size_t grow = static_cast<size_t>(bh) * p.Nk + key;
-        uint4* const outv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dv) + grow * D + h * (D / 2));
-        uint4* const outk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dk) + grow * D + h * (D / 2));
+        // dK and dV in bf16 are staged in the K and V buffers (free once
+        // acc_full has flipped) in the 128-byte swizzled box layout of their
+        // tensor maps, then one thread stores both tiles with TMA (keys past
+        // Nk are dropped)
+        const uint32_t stage_k = base + static_cast<uint32_t>(key_local) * 128u;
+        const uint32_t stage_v = stage_k + C::kTileBytes;
+        const uint32_t swz = static_cast<uint32_t>(key_local & 7);
 #pragma unroll
         for (int cc = 0; cc < D / 64; ++cc) {
+          const int col = h * (D / 2) + cc * 32;
+          const uint32_t off = static_cast<uint32_t>(col >> 6) * C::kBoxBytes;
+          const uint32_t chunk0 = static_cast<uint32_t>((col & 63) >> 3);
           uint32_t o[32];
           tmem_ld32(lane_base + kTmDV + h * (D / 2) + cc * 32, o);
           tmem_ld_wait(o);
           uint32_t w[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) w[i] = pack_bf16(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
-          if (store) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) outv[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-          }
+          for (int i = 0; i < 4; ++i)
+            st_shared_v4(stage_v + off + (((chunk0 + i) ^ swz) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2],
+                         w[4 * i + 3]);
           tmem_ld32(lane_base + kTmDK + h * (D / 2) + cc * 32, o);
           tmem_ld_wait(o);
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             w[i] = pack_bf16(__uint_as_float(o[2 * i]) * p.scale, __uint_as_float(o[2 * i + 1]) * p.scale);
-          if (store) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) outk[cc * 4 + i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          for (int i = 0; i < 4; ++i)
+            st_shared_v4(stage_k + off + (((chunk0 + i) ^ swz) << 4), w[4 * i], w[4 * i + 1], w[4 * i + 2],
+                         w[4 * i + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(7 + 2 * R));
+        if (threadIdx.x == 0) {
+          if (mbar_wait(bar(7 + 2 * R), 0, abort_flag)) {
+#pragma unroll
+            for (int b = 0; b < C::kBoxes; ++b) {
+              tma_store_3d(&tmDK, base + b * C::kBoxBytes, b * 64, key0, bh);
+              tma_store_3d(&tmDV, base + C::kTileBytes + b * C::kBoxBytes, b * 64, key0, bh);
+            }
+            bulk_commit_group();
+            bulk_wait_group_read0();
+          } else {
+            report_wait_failure(abort_flag, 8u);
           }
         }
       }
