@@ -90,6 +90,43 @@ def test_bwd_many_short_heads(d, causal):
            f"many heads d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("shape", [(333, 333, True), (333, 200, False), (77, 461, False)])
+def test_bwd_outputs_not_written_outside(d, shape):
+    """dQ, dK, dV embedded in larger guard-filled buffers: the guards stay
+    untouched and every gradient inside is finite.  The gradients go out
+    through tiled tensor stores of whole 128-row tiles; every head's last
+    tile here is ragged, so the stores must drop the rows past Nq (dQ) or Nk
+    (dK, dV) of each head."""
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    nq, nk, causal = shape
+    B, H = 2, 3
+    w = synth.Workload("bwd_guard", B, H, nq, nk, d, causal, seed=12)
+    q, k, v = w.make()
+    do = synth.normal_bf16(w.seed + 7, 3, w.q_shape())
+    tq, tk, tv, tdo = (to_device(x) for x in (q, k, v, do))
+    o, lse = fa.fwd(tq, tk, tv, causal=causal, scale=w.scale, n_splits=1)
+    pad = 4096
+
+    def guarded(n_rows):
+        big = torch.full((B * H * n_rows * d + 2 * pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+        return big, big[pad:pad + B * H * n_rows * d].view(B, H, n_rows, d)
+
+    (bq, dq), (bk, dk), (bv, dv) = guarded(nq), guarded(nk), guarded(nk)
+    fa.bwd(tq, tk, tv, o, lse, tdo, causal=causal, scale=w.scale, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    for big, t in ((bq, dq), (bk, dk), (bv, dv)):
+        assert torch.all(big[:pad] == 7.0) and torch.all(big[pad + t.numel():] == 7.0)
+        assert torch.isfinite(t).all()
+    ref = backward.attention_bwd(q, k, v, do, w.scale, causal)
+    got = tuple(t.float().cpu().numpy().astype(np.float64) for t in (dq, dk, dv))
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert _err(g, r) <= TOL, f"{name} normwise error {_err(g, r):.3e}"
+
+
 def test_bwd_deterministic():
     w = synth.Workload("bwd_det", 1, 3, 700, 700, 128, True, seed=830)
     q, k, v = w.make()

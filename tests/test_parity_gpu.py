@@ -211,24 +211,48 @@ def test_deterministic():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-def test_outputs_not_written_outside(d=128):
-    """O and LSE buffers embedded in larger guard-filled buffers: guards untouched."""
+@pytest.mark.parametrize("mode", ["causal_d128", "full_d128", "causal_d64_single_tile", "full_d64", "window_d128",
+                                  "split_d64", "split_causal_d128"])
+def test_outputs_not_written_outside(mode):
+    """O and LSE embedded in larger guard-filled buffers: the guards stay untouched.
+
+    O goes out through tiled tensor stores of whole 128-row tiles; the last
+    tile of every head here is ragged (333 rows), so the stores must drop the
+    rows past Nq of the last head (past the buffer) and of every other head
+    (the next head's rows).  Covers each kernel instantiation's epilogue."""
     import torch
 
     import exact_attention_19_gb300 as fa
 
-    w = synth.Workload("guard", 1, 2, 333, 333, d, True, seed=10)
+    d = 64 if "d64" in mode else 128
+    causal = "causal" in mode
+    B, H, N = 2, 3, 333
+    w = synth.Workload("guard", B, H, N, N, d, causal, seed=10)
     q, k, v = w.make()
     tq, tk, tv = to_device(q), to_device(k), to_device(v)
-    n_o = q.size
-    big_o = torch.full((n_o + 2 * 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
-    big_l = torch.full((2 * 333 + 2 * 64,), -3.0, dtype=torch.float32, device="cuda")
-    o = big_o[4096:4096 + n_o].view(q.shape)
-    lse = big_l[64:64 + 2 * 333].view(1, 2, 333)
-    fa.fwd(tq, tk, tv, causal=True, out=o, lse=lse)
+    n_o, n_l = q.size, B * H * N
+    pad_o, pad_l = 4096, 64
+    big_o = torch.full((n_o + 2 * pad_o,), 7.0, dtype=torch.bfloat16, device="cuda")
+    big_l = torch.full((n_l + 2 * pad_l,), -3.0, dtype=torch.float32, device="cuda")
+    o = big_o[pad_o:pad_o + n_o].view(q.shape)
+    lse = big_l[pad_l:pad_l + n_l].view(B, H, N)
+    kwargs = {}
+    if mode.startswith("window"):
+        kwargs["window"] = (100, 0)
+    elif mode.startswith("split"):
+        kwargs["n_splits"] = 3
+    else:
+        kwargs["n_splits"] = 1
+    fa.fwd(tq, tk, tv, causal=causal, scale=w.scale, out=o, lse=lse, **kwargs)
     torch.cuda.synchronize()
-    assert torch.all(big_o[:4096] == 7.0) and torch.all(big_o[4096 + n_o:] == 7.0)
-    assert torch.all(big_l[:64] == -3.0) and torch.all(big_l[64 + 666:] == -3.0)
+    assert torch.all(big_o[:pad_o] == 7.0) and torch.all(big_o[pad_o + n_o:] == 7.0)
+    assert torch.all(big_l[:pad_l] == -3.0) and torch.all(big_l[pad_l + n_l:] == -3.0)
+    # every row inside was written (and is right) -- spot-check against the oracle
+    rows = np.array([0, 127, 128, N - 1, N, 2 * N - 1, n_l - 1])
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, rows, w.scale, causal, window=kwargs.get("window"))
+    o_s = o.float().cpu().numpy().astype(np.float64).reshape(-1, d)[rows]
+    l_s = lse.cpu().numpy().astype(np.float64).reshape(-1)[rows]
+    assert_close(o_s, l_s, o_ref, lse_ref, mode)
 
 
 # --- device-side argument errors -------------------------------------------------
