@@ -74,7 +74,10 @@ bool set_smem_attrs() {
             set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
-  if constexpr (D == 64) ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess;
+  if constexpr (D == 64)
+    ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess &&
+         set_smem_attr<64, fa::kMaskNone, true, 1>() == cudaSuccess &&
+         set_smem_attr<64, fa::kMaskCausal, true, 1>() == cudaSuccess;
   return ok;
 }
 
@@ -348,10 +351,22 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   p.split_tiles = tiles;
   p.o_part = static_cast<float*>(workspace);
   p.lse_part = p.o_part + static_cast<size_t>(eff) * p.rows * d;
+  // d = 64: one query tile per CTA (two CTAs per SM) when the grid of
+  // query-tile pairs would leave more than half of the SMs idle or spill into
+  // a second wave; single tiles double the CTAs and halve each one's work
+  const long long pair_grid = static_cast<long long>(B) * H * p.n_pairs * eff;
+  const int sms = g_dev_sms_or(dev, 148);
+  const bool single = d == 64 && (2 * pair_grid < sms || pair_grid > sms);
+  if (single) p.n_pairs = (Nq + 127) / 128;
   const long long grid = static_cast<long long>(B) * H * p.n_pairs * eff;
   if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
-  const int rc = d == 64 ? launch_d<64, true>(causal, mq, mk, mv, mo, p, grid, stream)
-                         : launch_d<128, true>(causal, mq, mk, mv, mo, p, grid, stream);
+  int rc;
+  if (single)
+    rc = causal ? launch<64, fa::kMaskCausal, true, 1>(mq, mk, mv, mo, p, grid, stream)
+                : launch<64, fa::kMaskNone, true, 1>(mq, mk, mv, mo, p, grid, stream);
+  else
+    rc = d == 64 ? launch_d<64, true>(causal, mq, mk, mv, mo, p, grid, stream)
+                 : launch_d<128, true>(causal, mq, mk, mv, mo, p, grid, stream);
   if (rc != FA_OK) return rc;
   // The merge is a programmatic dependent launch: its CTAs may be scheduled
   // while the sliced kernel's last CTAs run, and wait in the kernel for its

@@ -107,6 +107,9 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* l
  * run and waits on the device for its completion), so stream order and the
  * results are those of two plain launches:
  *   L = log2 sum_s 2^L_s,   O = sum_s 2^(L_s - L) O_s,   LSE = L * ln 2.
+ * At d = 64 a CTA takes one query tile instead of two when the CTAs of tile
+ * pairs would fill under half of the multiprocessors or more than all of
+ * them; the slices, and so the results, are the same either way.
  *
  * Arguments as in fa_fwd, plus:
  * n_splits   requested slices, 1..64; the call uses ceil(n_kv / ceil(n_kv /

@@ -92,6 +92,22 @@ def test_splitkv_forced(n_splits, d, causal):
     _check_full(synth.Workload("split", 2, 3, 1000, 1000, d, causal, seed=71), n_splits)
 
 
+# d = 64 split-KV launches one query tile per CTA when the grid of tile pairs x
+# slices would fill under half of the SMs or more than all of them, else pairs;
+# these shapes land on each side on a 148- to 152-SM part
+@pytest.mark.parametrize("shape", [
+    (1, 1, 4096, False, 8),   # 128 pair CTAs: pairs
+    (1, 1, 1000, False, 3),   # 12: single tiles
+    (1, 3, 333, True, 2),     # 12: single tiles, causal (light tiles see one slice)
+    (2, 1, 4097, False, 5),   # 170 > SMs: single tiles, one-row ragged tail
+    (1, 1, 1024, True, 4),    # 16: single tiles, causal
+    (2, 4, 2048, False, 2),   # 128: pairs
+])
+def test_splitkv_cta_shapes(shape):
+    B, H, n, causal, n_splits = shape
+    _check_full(synth.Workload(f"split_cta{n}", B, H, n, n, 64, causal, seed=73 + n), n_splits)
+
+
 @pytest.mark.parametrize("d", [64, 128])
 def test_splitkv_wide_logits(d):
     # the merge weights 2^(L_s - L) span many orders of magnitude
