@@ -21,8 +21,10 @@
 // warps per SM sub-partition keep twice the exponentials in flight.  Each half
 // writes its bf16 results into its own columns (64h..64h+31), so no half
 // overwrites values the other has yet to read; the MMAs take their A operand
-// from columns 64 (kk / 4) + 8 (kk % 4).  Every wait is bounded as in the
-// forward kernel.
+// from columns 64 (kk / 4) + 8 (kk % 4).  The gradients leave through TMA
+// tensor stores, staged in bf16 in the resident tiles' buffers (Q for dQ, K and
+// V for dK and dV) once the last MMA has read them.  Every wait is bounded as
+// in the forward kernel.
 #pragma once
 
 #include <cstdint>
