@@ -17,8 +17,12 @@
  *   dQ = dS K * scale
  *   dK = dS^T Q * scale
  *
- * Masked scores (causal: key j kept for row i iff j <= i) have P = 0 and
- * therefore dS = 0.  Everything is recomputed from Q, K, V and dO in double
+ * Masked scores have P = 0 and therefore dS = 0.  Masks: causal (key j kept
+ * for row i iff j <= i), or a sliding window (wl, wr) aligned bottom-right as
+ * in the forward oracle: key j kept iff i + s - wl <= j <= i + s + wr with
+ * s = Nk - Nq, a negative bound leaving that side open.  A row that keeps no
+ * key has P = 0, O = 0 and D = 0, so it adds nothing to any gradient and its
+ * dQ is 0.  Everything is recomputed from Q, K, V and dO in double
  * precision: S, P, O and D of each row are materialised, no tiling, sums in
  * ascending index order.  bf16 inputs are widened exactly.
  *
@@ -46,39 +50,55 @@ static double elem(const void* base, int dtype, size_t idx) {
   return ((const double*)base)[idx];
 }
 
+enum { MASK_NONE = 0, MASK_CAUSAL = 1, MASK_WINDOW = 2 };
+
+/* The keys query row i keeps: [*lo_out, returned end). */
+static long visible_keys(long i, long Nq, long Nk, int mask, long wl, long wr, long* lo_out) {
+  const int causal = (mask == MASK_CAUSAL);
+  long lo = 0, n = Nk;
+  if (causal && i + 1 < Nk) n = i + 1;
+  if (mask == MASK_WINDOW) {
+    const long s = Nk - Nq;
+    if (wl >= 0 && i + s - wl > lo) lo = i + s - wl;
+    if (wr >= 0 && i + s + wr + 1 < n) n = i + s + wr + 1;
+  }
+  if (n < lo) n = lo;
+  *lo_out = lo;
+  return n;
+}
+
 /*
  * P row, dP row, O row and D of query row i of one head (base offsets of the
- * head given).  p_row, dp_row: length Nk scratch; o_row: length d scratch.
- * Returns the number of visible keys (keys 0 .. n-1).
+ * head given), over its visible keys [lo, n).  p_row, dp_row: length Nk
+ * scratch indexed by key; o_row: length d scratch.
  */
-static long row_state(const void* q, const void* k, const void* v, const void* dout, int dtype,
-                      size_t q_base, size_t kv_base, long i, long Nk, long d, double scale, int causal,
-                      double* p_row, double* dp_row, double* o_row, double* D_out) {
-  long n = Nk;
-  if (causal && i + 1 < Nk) n = i + 1;
-  if (n <= 0) {
+static void row_state(const void* q, const void* k, const void* v, const void* dout, int dtype, size_t q_base,
+                      size_t kv_base, long lo, long n, long d, double scale, double* p_row, double* dp_row,
+                      double* o_row, double* D_out) {
+  if (n <= lo) {
+    for (long c = 0; c < d; ++c) o_row[c] = 0.0;
     *D_out = 0.0;
-    return 0;
+    return;
   }
   /* S row and its safe softmax */
-  for (long j = 0; j < n; ++j) {
+  for (long j = lo; j < n; ++j) {
     double dot = 0.0;
     for (long c = 0; c < d; ++c)
       dot += elem(q, dtype, q_base + (size_t)c) * elem(k, dtype, kv_base + (size_t)j * (size_t)d + (size_t)c);
     p_row[j] = scale * dot;
   }
-  double m = p_row[0];
-  for (long j = 1; j < n; ++j)
+  double m = p_row[lo];
+  for (long j = lo + 1; j < n; ++j)
     if (p_row[j] > m) m = p_row[j];
   double l = 0.0;
-  for (long j = 0; j < n; ++j) {
+  for (long j = lo; j < n; ++j) {
     p_row[j] = exp(p_row[j] - m);
     l += p_row[j];
   }
-  for (long j = 0; j < n; ++j) p_row[j] /= l;
+  for (long j = lo; j < n; ++j) p_row[j] /= l;
   /* O row = P V; dP row = dO_i V^T; D = dO_i . O_i */
   for (long c = 0; c < d; ++c) o_row[c] = 0.0;
-  for (long j = 0; j < n; ++j) {
+  for (long j = lo; j < n; ++j) {
     double dp = 0.0;
     for (long c = 0; c < d; ++c) {
       const double vjc = elem(v, dtype, kv_base + (size_t)j * (size_t)d + (size_t)c);
@@ -90,7 +110,6 @@ static long row_state(const void* q, const void* k, const void* v, const void* d
   double D = 0.0;
   for (long c = 0; c < d; ++c) D += elem(dout, dtype, q_base + (size_t)c) * o_row[c];
   *D_out = D;
-  return n;
 }
 
 int oracle_bwd_threads(void) {
@@ -106,9 +125,9 @@ int oracle_bwd_threads(void) {
  * k, v [B,H,Nk,d], dout [B,H,Nq,d].  Heads run in parallel; inside a head the
  * rows are visited in order and dK, dV accumulate in that order.
  */
-int oracle_attention_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype, double* dq,
-                         double* dk, double* dv, long long B, long long H, long long Nq, long long Nk,
-                         long long d, double scale, int causal, int nthreads) {
+static int bwd_all(const void* q, const void* k, const void* v, const void* dout, int dtype, double* dq,
+                   double* dk, double* dv, long long B, long long H, long long Nq, long long Nk, long long d,
+                   double scale, int mask, long wl, long wr, int nthreads) {
   if (!q || !k || !v || !dout || !dq || !dk || !dv) return -1;
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d <= 0) return -2;
   if (dtype != BWD_F64 && dtype != BWD_BF16) return -3;
@@ -137,11 +156,12 @@ int oracle_attention_bwd(const void* q, const void* k, const void* v, const void
         for (long long i = 0; i < Nq; ++i) {
           const size_t q_base = ((size_t)bh * (size_t)Nq + (size_t)i) * (size_t)d;
           double D;
-          const long n = row_state(q, k, v, dout, dtype, q_base, kv_base, (long)i, (long)Nk, (long)d, scale, causal,
-                                   p_row, dp_row, o_row, &D);
+          long lo;
+          const long n = visible_keys((long)i, (long)Nq, (long)Nk, mask, wl, wr, &lo);
+          row_state(q, k, v, dout, dtype, q_base, kv_base, lo, n, (long)d, scale, p_row, dp_row, o_row, &D);
           double* dq_row = dq + q_base;
           for (long c = 0; c < d; ++c) dq_row[c] = 0.0;
-          for (long j = 0; j < n; ++j) {
+          for (long j = lo; j < n; ++j) {
             const double ds = p_row[j] * (dp_row[j] - D);
             const size_t krow = kv_base + (size_t)j * (size_t)d;
             for (long c = 0; c < d; ++c) {
@@ -165,10 +185,10 @@ int oracle_attention_bwd(const void* q, const void* k, const void* v, const void
 /*
  * dQ for selected query rows (flat index (b*H + h)*Nq + i): dq_rows [n_rows, d].
  */
-int oracle_attention_bwd_dq_rows(const void* q, const void* k, const void* v, const void* dout, int dtype,
-                                 const long long* rows, long long n_rows, double* dq_rows, long long B,
-                                 long long H, long long Nq, long long Nk, long long d, double scale, int causal,
-                                 int nthreads) {
+static int bwd_dq_rows(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                       const long long* rows, long long n_rows, double* dq_rows, long long B, long long H,
+                       long long Nq, long long Nk, long long d, double scale, int mask, long wl, long wr,
+                       int nthreads) {
   if (!q || !k || !v || !dout || !dq_rows || (!rows && n_rows > 0)) return -1;
   const long long total = B * H * Nq;
   for (long long r = 0; r < n_rows; ++r)
@@ -194,11 +214,12 @@ int oracle_attention_bwd_dq_rows(const void* q, const void* k, const void* v, co
         const size_t kv_base = (size_t)bh * (size_t)Nk * (size_t)d;
         const size_t q_base = (size_t)rows[r] * (size_t)d;
         double D;
-        const long n = row_state(q, k, v, dout, dtype, q_base, kv_base, (long)i, (long)Nk, (long)d, scale, causal,
-                                 p_row, dp_row, o_row, &D);
+        long lo;
+        const long n = visible_keys((long)i, (long)Nq, (long)Nk, mask, wl, wr, &lo);
+        row_state(q, k, v, dout, dtype, q_base, kv_base, lo, n, (long)d, scale, p_row, dp_row, o_row, &D);
         double* out = dq_rows + (size_t)r * (size_t)d;
         for (long c = 0; c < d; ++c) out[c] = 0.0;
-        for (long j = 0; j < n; ++j) {
+        for (long j = lo; j < n; ++j) {
           const double ds = p_row[j] * (dp_row[j] - D);
           for (long c = 0; c < d; ++c) out[c] += ds * elem(k, dtype, kv_base + (size_t)j * (size_t)d + (size_t)c);
         }
@@ -218,10 +239,10 @@ int oracle_attention_bwd_dq_rows(const void* q, const void* k, const void* v, co
  * the head is visited (its P row, dP row and D recomputed), and the selected
  * columns are accumulated in query order.
  */
-int oracle_attention_bwd_dkdv_keys(const void* q, const void* k, const void* v, const void* dout, int dtype,
-                                   long long bh, const long long* keys, long long n_keys, double* dk_rows,
-                                   double* dv_rows, long long B, long long H, long long Nq, long long Nk,
-                                   long long d, double scale, int causal, int nthreads) {
+static int bwd_dkdv_keys(const void* q, const void* k, const void* v, const void* dout, int dtype, long long bh,
+                         const long long* keys, long long n_keys, double* dk_rows, double* dv_rows, long long B,
+                         long long H, long long Nq, long long Nk, long long d, double scale, int mask, long wl,
+                         long wr, int nthreads) {
   if (!q || !k || !v || !dout || !dk_rows || !dv_rows || (!keys && n_keys > 0)) return -1;
   if (bh < 0 || bh >= B * H) return -4;
   for (long long t = 0; t < n_keys; ++t)
@@ -254,13 +275,15 @@ int oracle_attention_bwd_dkdv_keys(const void* q, const void* k, const void* v, 
       for (long long i = 0; i < Nq; ++i) {
         const size_t q_base = ((size_t)bh * (size_t)Nq + (size_t)i) * (size_t)d;
         double D;
-        const long n = row_state(q, k, v, dout, dtype, q_base, kv_base, (long)i, (long)Nk, (long)d, scale, causal,
-                                 p_row, dp_row, o_row, &D);
+        long lo;
+        const long n = visible_keys((long)i, (long)Nq, (long)Nk, mask, wl, wr, &lo);
+        row_state(q, k, v, dout, dtype, q_base, kv_base, lo, n, (long)d, scale, p_row, dp_row, o_row, &D);
         for (long long t = 0; t < n_keys; ++t) {
           const long j = (long)keys[t];
-          const double pj = j < n ? p_row[j] : 0.0;
+          const int kept = j >= lo && j < n;
+          const double pj = kept ? p_row[j] : 0.0;
           p_sel[(size_t)i * (size_t)n_keys + (size_t)t] = pj;
-          ds_sel[(size_t)i * (size_t)n_keys + (size_t)t] = j < n ? pj * (dp_row[j] - D) : 0.0;
+          ds_sel[(size_t)i * (size_t)n_keys + (size_t)t] = kept ? pj * (dp_row[j] - D) : 0.0;
         }
       }
     }
@@ -288,4 +311,54 @@ int oracle_attention_bwd_dkdv_keys(const void* q, const void* k, const void* v, 
   free(ds_sel);
   free(p_sel);
   return failed ? -5 : 0;
+}
+
+/* Public entry points.  causal: 0 or 1.  The _window forms take the window
+ * (wl, wr) aligned bottom-right; a negative bound leaves that side open. */
+int oracle_attention_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype, double* dq,
+                         double* dk, double* dv, long long B, long long H, long long Nq, long long Nk,
+                         long long d, double scale, int causal, int nthreads) {
+  return bwd_all(q, k, v, dout, dtype, dq, dk, dv, B, H, Nq, Nk, d, scale, causal ? MASK_CAUSAL : MASK_NONE, -1,
+                 -1, nthreads);
+}
+
+int oracle_attention_bwd_window(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                                double* dq, double* dk, double* dv, long long B, long long H, long long Nq,
+                                long long Nk, long long d, double scale, long long wl, long long wr,
+                                int nthreads) {
+  return bwd_all(q, k, v, dout, dtype, dq, dk, dv, B, H, Nq, Nk, d, scale, MASK_WINDOW, (long)wl, (long)wr,
+                 nthreads);
+}
+
+int oracle_attention_bwd_dq_rows(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                                 const long long* rows, long long n_rows, double* dq_rows, long long B,
+                                 long long H, long long Nq, long long Nk, long long d, double scale, int causal,
+                                 int nthreads) {
+  return bwd_dq_rows(q, k, v, dout, dtype, rows, n_rows, dq_rows, B, H, Nq, Nk, d, scale,
+                     causal ? MASK_CAUSAL : MASK_NONE, -1, -1, nthreads);
+}
+
+int oracle_attention_bwd_dq_rows_window(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                                        const long long* rows, long long n_rows, double* dq_rows, long long B,
+                                        long long H, long long Nq, long long Nk, long long d, double scale,
+                                        long long wl, long long wr, int nthreads) {
+  return bwd_dq_rows(q, k, v, dout, dtype, rows, n_rows, dq_rows, B, H, Nq, Nk, d, scale, MASK_WINDOW, (long)wl,
+                     (long)wr, nthreads);
+}
+
+int oracle_attention_bwd_dkdv_keys(const void* q, const void* k, const void* v, const void* dout, int dtype,
+                                   long long bh, const long long* keys, long long n_keys, double* dk_rows,
+                                   double* dv_rows, long long B, long long H, long long Nq, long long Nk,
+                                   long long d, double scale, int causal, int nthreads) {
+  return bwd_dkdv_keys(q, k, v, dout, dtype, bh, keys, n_keys, dk_rows, dv_rows, B, H, Nq, Nk, d, scale,
+                       causal ? MASK_CAUSAL : MASK_NONE, -1, -1, nthreads);
+}
+
+int oracle_attention_bwd_dkdv_keys_window(const void* q, const void* k, const void* v, const void* dout,
+                                          int dtype, long long bh, const long long* keys, long long n_keys,
+                                          double* dk_rows, double* dv_rows, long long B, long long H,
+                                          long long Nq, long long Nk, long long d, double scale, long long wl,
+                                          long long wr, int nthreads) {
+  return bwd_dkdv_keys(q, k, v, dout, dtype, bh, keys, n_keys, dk_rows, dv_rows, B, H, Nq, Nk, d, scale,
+                       MASK_WINDOW, (long)wl, (long)wr, nthreads);
 }

@@ -38,6 +38,15 @@ def _declare(lib):
     lib.oracle_attention_bwd_dkdv_keys.argtypes = [vp, vp, vp, vp, ci, i64, vp, i64, vp, vp, i64, i64, i64, i64,
                                                    i64, ctypes.c_double, ci, ci]
     lib.oracle_attention_bwd_dkdv_keys.restype = ci
+    lib.oracle_attention_bwd_window.argtypes = [vp, vp, vp, vp, ci, vp, vp, vp, i64, i64, i64, i64, i64,
+                                                ctypes.c_double, i64, i64, ci]
+    lib.oracle_attention_bwd_window.restype = ci
+    lib.oracle_attention_bwd_dq_rows_window.argtypes = [vp, vp, vp, vp, ci, vp, i64, vp, i64, i64, i64, i64, i64,
+                                                        ctypes.c_double, i64, i64, ci]
+    lib.oracle_attention_bwd_dq_rows_window.restype = ci
+    lib.oracle_attention_bwd_dkdv_keys_window.argtypes = [vp, vp, vp, vp, ci, i64, vp, i64, vp, vp, i64, i64, i64,
+                                                          i64, i64, ctypes.c_double, i64, i64, ci]
+    lib.oracle_attention_bwd_dkdv_keys_window.restype = ci
     return lib
 
 
@@ -67,8 +76,12 @@ def _prep(arrs):
     return out, kinds.pop()
 
 
-def attention_bwd(q, k, v, dout, scale, causal=False, nthreads=0, lib=None):
-    """(dq [B,H,Nq,d], dk [B,H,Nk,d], dv [B,H,Nk,d]) in float64."""
+def attention_bwd(q, k, v, dout, scale, causal=False, nthreads=0, lib=None, window=None):
+    """(dq [B,H,Nq,d], dk [B,H,Nk,d], dv [B,H,Nk,d]) in float64.
+
+    window=(wl, wr): key j kept for row i iff i + s - wl <= j <= i + s + wr,
+    s = Nk - Nq (aligned bottom-right), a negative bound leaving that side
+    open; causal is then ignored."""
     lib = lib or load_library()
     (q, k, v, dout), kind = _prep([q, k, v, dout])
     B, H, Nq, d = q.shape
@@ -76,32 +89,43 @@ def attention_bwd(q, k, v, dout, scale, causal=False, nthreads=0, lib=None):
     dq = np.zeros(q.shape)
     dk = np.zeros(k.shape)
     dv = np.zeros(v.shape)
-    rc = lib.oracle_attention_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, kind,
-                                  dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, B, H, Nq, Nk, d, float(scale),
-                                  int(bool(causal)), int(nthreads))
+    if window is not None:
+        rc = lib.oracle_attention_bwd_window(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, kind,
+                                             dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, B, H, Nq, Nk, d,
+                                             float(scale), int(window[0]), int(window[1]), int(nthreads))
+    else:
+        rc = lib.oracle_attention_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, kind,
+                                      dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, B, H, Nq, Nk, d,
+                                      float(scale), int(bool(causal)), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attention_bwd failed ({rc})")
     return dq, dk, dv
 
 
-def attention_bwd_dq_rows(q, k, v, dout, rows, scale, causal=False, nthreads=0, lib=None):
-    """dQ of selected flat query rows (b*H + h)*Nq + i: [len(rows), d]."""
+def attention_bwd_dq_rows(q, k, v, dout, rows, scale, causal=False, nthreads=0, lib=None, window=None):
+    """dQ of selected flat query rows (b*H + h)*Nq + i: [len(rows), d]; window as in attention_bwd."""
     lib = lib or load_library()
     (q, k, v, dout), kind = _prep([q, k, v, dout])
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     out = np.zeros((rows.size, d))
-    rc = lib.oracle_attention_bwd_dq_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, kind,
-                                          rows.ctypes.data, rows.size, out.ctypes.data, B, H, Nq, Nk, d,
-                                          float(scale), int(bool(causal)), int(nthreads))
+    if window is not None:
+        rc = lib.oracle_attention_bwd_dq_rows_window(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+                                                     kind, rows.ctypes.data, rows.size, out.ctypes.data, B, H, Nq,
+                                                     Nk, d, float(scale), int(window[0]), int(window[1]),
+                                                     int(nthreads))
+    else:
+        rc = lib.oracle_attention_bwd_dq_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, kind,
+                                              rows.ctypes.data, rows.size, out.ctypes.data, B, H, Nq, Nk, d,
+                                              float(scale), int(bool(causal)), int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attention_bwd_dq_rows failed ({rc})")
     return out
 
 
-def attention_bwd_dkdv_keys(q, k, v, dout, bh, keys, scale, causal=False, nthreads=0, lib=None):
-    """dK and dV rows of selected keys of head bh: ([len(keys), d], [len(keys), d])."""
+def attention_bwd_dkdv_keys(q, k, v, dout, bh, keys, scale, causal=False, nthreads=0, lib=None, window=None):
+    """dK and dV rows of selected keys of head bh: ([len(keys), d], [len(keys), d]); window as in attention_bwd."""
     lib = lib or load_library()
     (q, k, v, dout), kind = _prep([q, k, v, dout])
     B, H, Nq, d = q.shape
@@ -109,9 +133,16 @@ def attention_bwd_dkdv_keys(q, k, v, dout, bh, keys, scale, causal=False, nthrea
     keys = np.ascontiguousarray(keys, dtype=np.int64)
     dk = np.zeros((keys.size, d))
     dv = np.zeros((keys.size, d))
-    rc = lib.oracle_attention_bwd_dkdv_keys(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, kind,
-                                            int(bh), keys.ctypes.data, keys.size, dk.ctypes.data, dv.ctypes.data,
-                                            B, H, Nq, Nk, d, float(scale), int(bool(causal)), int(nthreads))
+    if window is not None:
+        rc = lib.oracle_attention_bwd_dkdv_keys_window(q.ctypes.data, k.ctypes.data, v.ctypes.data,
+                                                       dout.ctypes.data, kind, int(bh), keys.ctypes.data, keys.size,
+                                                       dk.ctypes.data, dv.ctypes.data, B, H, Nq, Nk, d, float(scale),
+                                                       int(window[0]), int(window[1]), int(nthreads))
+    else:
+        rc = lib.oracle_attention_bwd_dkdv_keys(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data,
+                                                kind, int(bh), keys.ctypes.data, keys.size, dk.ctypes.data,
+                                                dv.ctypes.data, B, H, Nq, Nk, d, float(scale), int(bool(causal)),
+                                                int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attention_bwd_dkdv_keys failed ({rc})")
     return dk, dv

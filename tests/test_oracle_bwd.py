@@ -31,7 +31,15 @@ MUTANTS = {
     "causal_off_by_one": ("if (causal && i + 1 < Nk) n = i + 1;", "if (causal && i + 2 < Nk) n = i + 2;"),
     "dk_uses_k": ("dk_h[(size_t)j * (size_t)d + (size_t)c] += ds * elem(q, dtype, q_base + (size_t)c);",
                   "dk_h[(size_t)j * (size_t)d + (size_t)c] += ds * elem(k, dtype, krow + (size_t)c);"),
-    "softmax_unnormalised": ("for (long j = 0; j < n; ++j) p_row[j] /= l;", "(void)l;"),
+    "softmax_unnormalised": ("for (long j = lo; j < n; ++j) p_row[j] /= l;", "(void)l;"),
+    "window_left_off_by_one": ("if (wl >= 0 && i + s - wl > lo) lo = i + s - wl;",
+                               "if (wl >= 0 && i + s - wl + 1 > lo) lo = i + s - wl + 1;"),
+    "window_right_off_by_one": ("if (wr >= 0 && i + s + wr + 1 < n) n = i + s + wr + 1;",
+                                "if (wr >= 0 && i + s + wr < n) n = i + s + wr;"),
+    "window_top_left": ("const long s = Nk - Nq;", "const long s = 0;"),
+    "window_sides_swapped": ("if (wl >= 0 && i + s - wl > lo) lo = i + s - wl;",
+                             "if (wr >= 0 && i + s - wr > lo) lo = i + s - wr;"),
+    "empty_window_sees_all": ("  if (n < lo) n = lo;", "  if (n < lo) {\n    lo = 0;\n    n = Nk;\n  }"),
 }
 
 
