@@ -21,7 +21,7 @@ __all__ = [
     "FaError", "STATUS", "NOALLOC_SCRATCH_BYTES", "library_path", "load",
     "fwd", "bwd",
     "fa_fwd", "fa_fwd_window", "fa_fwd_splitkv", "fa_fwd_splitkv_noalloc", "fa_splitkv_workspace_bytes",
-    "fa_splitkv_heuristic", "fa_bwd", "fa_bwd_workspace_bytes", "fa_probe_exp2", "fa_selftest_wait",
+    "fa_splitkv_heuristic", "fa_bwd", "fa_bwd_window", "fa_bwd_workspace_bytes", "fa_probe_exp2", "fa_selftest_wait",
     "fa_fwd_status",
     "fa_strerror", "fa_version",
 ]
@@ -86,6 +86,9 @@ def load():
         lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32, vp,
                                ctypes.c_size_t, vp]
         lib.fa_bwd.restype = i32
+        lib.fa_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float, i32,
+                                      i32, vp, ctypes.c_size_t, vp]
+        lib.fa_bwd_window.restype = i32
         lib.fa_bwd_workspace_bytes.argtypes = [i32, i32, i32]
         lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
         _lib = lib
@@ -146,6 +149,14 @@ def fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, causal, wo
     """Raw C-ABI backward call; returns the status code (does not raise)."""
     return int(load().fa_bwd(q, k, v, o, lse, dout, dq, dk, dv, int(B), int(H), int(Nq), int(Nk), int(d),
                              float(scale), int(causal), workspace, int(workspace_bytes), stream))
+
+
+def fa_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, window_left, window_right, workspace,
+                  workspace_bytes, stream) -> int:
+    """Raw C-ABI sliding-window backward call (bottom-right aligned, -1 = unbounded); returns the status code."""
+    return int(load().fa_bwd_window(q, k, v, o, lse, dout, dq, dk, dv, int(B), int(H), int(Nq), int(Nk), int(d),
+                                    float(scale), int(window_left), int(window_right), workspace,
+                                    int(workspace_bytes), stream))
 
 
 def fa_bwd_workspace_bytes(B, H, Nq) -> int:
@@ -253,12 +264,14 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse
 
 
 def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
-        workspace=None, stream=None):
+        workspace=None, stream=None, window: tuple | None = None):
     """(dq, dk, dv) of attention by recomputation from the forward's ``lse``.
 
     q, o, dout: [B, H, Nq, d]; k, v: [B, H, Nk, d], CUDA bf16, contiguous;
     lse: fp32 [B, H, Nq] from ``fwd``.  ``workspace`` (CUDA tensor of at least
     ``fa_bwd_workspace_bytes`` bytes) may be given to avoid allocating it.
+    ``window=(left, right)``: the sliding-window mask of ``fwd(window=...)``
+    (pass the same window to both; ``causal`` is then ignored).
     """
     import torch
 
@@ -283,9 +296,17 @@ def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
     need = fa_bwd_workspace_bytes(B, H, Nq)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    if window is not None:
+        st = fa_bwd_window(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
+                           dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, scale, int(window[0]),
+                           int(window[1]), workspace.data_ptr(), ws_bytes, _stream_handle(stream))
+        if st != 0:
+            raise FaError(st, "fa_bwd_window")
+        return dq, dk, dv
     st = fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), dout.data_ptr(),
                 dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Nq, Nk, d, scale, int(bool(causal)),
-                workspace.data_ptr(), workspace.numel() * workspace.element_size(), _stream_handle(stream))
+                workspace.data_ptr(), ws_bytes, _stream_handle(stream))
     if st != 0:
         raise FaError(st, "fa_bwd")
     return dq, dk, dv

@@ -54,17 +54,19 @@ cudaError_t set_smem_attr() {
                               static_cast<int>(fa::Cfg<D, TILES>::kSmemBytes));
 }
 
+template <int D, int MASK>
+bool set_bwd_smem_attr() {
+  using C = fa::BwdCfg<D>;
+  return cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(C::kSmemQ)) == cudaSuccess &&
+         cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(C::kSmemKV)) == cudaSuccess;
+}
+
 template <int D>
 bool set_bwd_smem_attrs() {
-  using C = fa::BwdCfg<D>;
-  return cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(C::kSmemQ)) == cudaSuccess &&
-         cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(C::kSmemQ)) == cudaSuccess &&
-         cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(C::kSmemKV)) == cudaSuccess &&
-         cudaFuncSetAttribute(fa::fa_bwd_dkdv_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(C::kSmemKV)) == cudaSuccess;
+  return set_bwd_smem_attr<D, fa::kBwdMaskNone>() && set_bwd_smem_attr<D, fa::kBwdMaskCausal>() &&
+         set_bwd_smem_attr<D, fa::kBwdMaskWindow>();
 }
 
 template <int D>
@@ -159,15 +161,15 @@ int launch_d(bool causal, const CUtensorMap& mq, const CUtensorMap& mk, const CU
                 : launch<D, fa::kMaskNone, SPLIT>(mq, mk, mv, mo, p, grid, stream);
 }
 
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mdo,
                const CUtensorMap& mdq, const CUtensorMap& mdk, const CUtensorMap& mdv, const fa::BwdParams& p,
                long long bh, cudaStream_t stream) {
   using C = fa::BwdCfg<D>;
-  fa::fa_bwd_dq_kernel<D, CAUSAL><<<static_cast<unsigned>(bh * p.n_qt), C::kThreads, C::kSmemQ, stream>>>(
+  fa::fa_bwd_dq_kernel<D, MASK><<<static_cast<unsigned>(bh * p.n_qt), C::kThreads, C::kSmemQ, stream>>>(
       mq, mk, mv, mdo, mdq, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  fa::fa_bwd_dkdv_kernel<D, CAUSAL><<<static_cast<unsigned>(bh * p.n_kt), C::kThreads, C::kSmemKV, stream>>>(
+  fa::fa_bwd_dkdv_kernel<D, MASK><<<static_cast<unsigned>(bh * p.n_kt), C::kThreads, C::kSmemKV, stream>>>(
       mq, mk, mv, mdo, mdk, mdv, p);
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -447,9 +449,16 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq) {
   return 2 * static_cast<size_t>(B) * H * nq_pad * sizeof(float);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
-           void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal, void* workspace,
-           size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The backward under one of the three masks, with the checks shared by
+// fa_bwd and fa_bwd_window in the order fa.h documents (`causal` is fa_bwd's
+// argument, 0 for a window).
+int bwd_impl(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+             void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal, int mask,
+             int window_left, int window_right, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   const void* ptrs[] = {q, k, v, o, lse, dout, dq, dk, dv, workspace};
   for (const void* x : ptrs)
     if (!x) return FA_ERR_NULL;
@@ -492,11 +501,37 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
   p.dsum = p.lse2 + static_cast<size_t>(BH) * p.Nq_pad;
   p.scale = scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
-  if (d == 64)
-    return causal ? launch_bwd<64, true>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream)
-                  : launch_bwd<64, false>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream);
-  return causal ? launch_bwd<128, true>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream)
-                : launch_bwd<128, false>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream);
+  p.win_left = window_left;
+  p.win_right = window_right;
+  p.diag_off = Nk - Nq;  // bottom-right, as in the forward
+  if (mask == fa::kBwdMaskWindow)
+    return d == 64 ? launch_bwd<64, fa::kBwdMaskWindow>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream)
+                   : launch_bwd<128, fa::kBwdMaskWindow>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream);
+  if (mask == fa::kBwdMaskCausal)
+    return d == 64 ? launch_bwd<64, fa::kBwdMaskCausal>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream)
+                   : launch_bwd<128, fa::kBwdMaskCausal>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream);
+  return d == 64 ? launch_bwd<64, fa::kBwdMaskNone>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream)
+                 : launch_bwd<128, fa::kBwdMaskNone>(mq, mk, mv, mdo, mdq, mdk, mdv, p, BH, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+           void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal, void* workspace,
+           size_t workspace_bytes, cudaStream_t stream) {
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, causal,
+                  causal == 1 ? fa::kBwdMaskCausal : fa::kBwdMaskNone, -1, -1, workspace, workspace_bytes, stream);
+}
+
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int window_left,
+                  int window_right, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (window_left < -1 || window_right < -1) return FA_ERR_SHAPE;
+  const int mask = (window_left < 0 && window_right < 0) ? fa::kBwdMaskNone : fa::kBwdMaskWindow;
+  return bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, B, H, Nq, Nk, d, scale, 0, mask, window_left, window_right,
+                  workspace, workspace_bytes, stream);
 }
 
 int fa_fwd_status(cudaStream_t stream, unsigned int* detail, int clear) {

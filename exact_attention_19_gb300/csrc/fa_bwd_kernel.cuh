@@ -47,7 +47,15 @@ struct BwdParams {
   int n_qt, n_kt;     // query / key tiles per head
   float scale;        // softmax scale
   float scale_log2;   // scale * log2(e)
+  // window mask only: key j is kept for query row i iff
+  //   i + diag_off - win_left <= j <= i + diag_off + win_right  (a negative bound: that side open)
+  int win_left, win_right, diag_off;
 };
+
+// kBwdMaskCausal: key j kept for row i iff j <= i (Nq == Nk); kBwdMaskWindow:
+// the general window of BwdParams.  Each kernel then visits only the tiles its
+// rows (keys) can see; a tile that sees none writes zero gradients.
+enum : int { kBwdMaskNone = 0, kBwdMaskCausal = 1, kBwdMaskWindow = 2 };
 
 template <int D>
 struct BwdCfg {
@@ -81,7 +89,7 @@ struct BwdCfg {
 // barriers: 0 q_full, 1 s_full, 2 dp_full, 3 s_free, 4 ds_full, 5 dq_full,
 // 6 drain, 7..10 the D half-sum exchange (one per TMEM lane quarter), then
 // ring full[kRingQ], empty[kRingQ], then the epilogue's staging barrier
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -133,14 +141,30 @@ __global__ void __launch_bounds__(320, 1)
 
   const int bh = blockIdx.x / p.n_qt;
   int qt = blockIdx.x % p.n_qt;
-  if (CAUSAL) qt = p.n_qt - 1 - qt;  // heaviest tile of each head first
+  if (MASK == kBwdMaskCausal) qt = p.n_qt - 1 - qt;  // heaviest tile of each head first
   const int row0 = qt * 128;
   const int n_kv_all = (p.Nk + 127) / 128;
-  const int nkv = CAUSAL ? min(n_kv_all, qt + 1) : n_kv_all;
+  // visible K/V tiles [jlo, jlo + nkv) of this query tile; only a window
+  // can leave a tile with none (any_kv is a compile-time true otherwise)
+  int jlo = 0, nkv = n_kv_all;
+  if (MASK == kBwdMaskCausal) nkv = min(n_kv_all, qt + 1);
+  if (MASK == kBwdMaskWindow) {
+    const long long r_first = row0, r_last = min(row0 + 128, p.Nq) - 1;
+    long long key_lo = 0, key_hi = p.Nk - 1;
+    if (p.win_left >= 0) key_lo = max(0ll, r_first + p.diag_off - p.win_left);
+    if (p.win_right >= 0) key_hi = min(key_hi, r_last + p.diag_off + p.win_right);
+    if (key_lo > key_hi) {
+      nkv = 0;  // no row of this tile sees a key: dQ = 0
+    } else {
+      jlo = static_cast<int>(key_lo / 128);
+      nkv = static_cast<int>(key_hi / 128) + 1 - jlo;
+    }
+  }
+  const bool any_kv = MASK != kBwdMaskWindow || nkv > 0;
 
   if (warp == 8) {
     // ======================= TMA producer =================================
-    if (lane == 0) {
+    if (lane == 0 && any_kv) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
@@ -160,8 +184,8 @@ __global__ void __launch_bounds__(320, 1)
         if (!(ok = mbar_wait(empty(s), ((item / R) & 1) ^ 1u, abort_flag))) break;
         mbar_arrive_expect_tx(full(s), C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, (item & 1) ? &tmK : &tmV, full(s), b * 64, (item >> 1) * 128,
-                      bh);
+          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, (item & 1) ? &tmK : &tmV, full(s), b * 64,
+                      (jlo + (item >> 1)) * 128, bh);
       }
       if (!ok) report_wait_failure(abort_flag, 2u);
       if (*abort_flag) {
@@ -194,9 +218,9 @@ __global__ void __launch_bounds__(320, 1)
                  dRingMN + slot_off(s) + ((kk * 2048) >> 4), C::kIdescAcc, (acc_prev || kk > 0) ? 1u : 0u);
       };
       auto wait_item = [&](int it) -> bool { return mbar_wait(full(it % R), (it / R) & 1, abort_flag); };
-      // ring items: V_j = 2j, K_j = 2j + 1
-      bool ok = mbar_wait(bar(0), 0, abort_flag) && wait_item(0) && wait_item(1);
-      if (ok) {
+      // ring items: V_j = 2j, K_j = 2j + 1 (tile jlo + j)
+      bool ok = !any_kv || (mbar_wait(bar(0), 0, abort_flag) && wait_item(0) && wait_item(1));
+      if (ok && any_kv) {
         tc_fence_after();
         score(dQd, 1, kTmS);
         mma_commit(bar(1));
@@ -282,6 +306,18 @@ __global__ void __launch_bounds__(320, 1)
     const float POS_INF = __int_as_float(0x7f800000);
     const bool valid = row < p.Nq;
     const size_t grow = static_cast<size_t>(bh) * p.Nq + row;
+    // keys [row_key_lo, row_key_end) are visible to this row (window bounds
+    // clamped into [-1, Nk], so every later difference fits an int)
+    int row_key_lo = 0, row_key_end = p.Nk;
+    if (MASK == kBwdMaskCausal) row_key_end = min(p.Nk, row + 1);
+    if (MASK == kBwdMaskWindow) {
+      if (p.win_left >= 0)
+        row_key_lo = static_cast<int>(min(static_cast<long long>(p.Nk),
+                                          max(-1ll, static_cast<long long>(row) + p.diag_off - p.win_left)));
+      if (p.win_right >= 0)
+        row_key_end = static_cast<int>(
+            min(static_cast<long long>(p.Nk), max(-1ll, static_cast<long long>(row) + p.diag_off + p.win_right) + 1));
+    }
     // D = rowsum(dO * O) in fp32, L = LSE * log2(e); padding rows: P = 0.
     // Each half sums its own D/2 columns with every load issued up front (one
     // memory round trip), then the two half sums meet in shared memory and
@@ -345,18 +381,25 @@ __global__ void __launch_bounds__(320, 1)
       tc_fence_before();
       mbar_arrive(bar(3));
       float* const f[2] = {reinterpret_cast<float*>(s0), reinterpret_cast<float*>(s1)};
-      // visible columns of this half [0, lim): ragged key tail and the causal diagonal
-      int lim = p.Nk;
-      if (CAUSAL) lim = min(lim, row + 1);
-      lim -= j * 128 + h * 64;
+      // visible columns of this half [lo, lim): ragged key tail, the causal
+      // diagonal or the window's two edges
+      const int col0 = (jlo + j) * 128 + h * 64;
+      const int lim = row_key_end - col0;
+      const int lo = (MASK == kBwdMaskWindow) ? row_key_lo - col0 : 0;
 #pragma unroll
       for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float x0, x1;
           fma2(x0, x1, f[q2][i], f[q2][i + 1], c, neg_lse2);
-          f[q2][i] = (q2 * 32 + i < lim) ? ex2(x0) : 0.f;
-          f[q2][i + 1] = (q2 * 32 + i + 1 < lim) ? ex2(x1) : 0.f;
+          const int e = q2 * 32 + i;
+          if (MASK == kBwdMaskWindow) {
+            f[q2][i] = (e < lim && e >= lo) ? ex2(x0) : 0.f;
+            f[q2][i + 1] = (e + 1 < lim && e + 1 >= lo) ? ex2(x1) : 0.f;
+          } else {
+            f[q2][i] = (e < lim) ? ex2(x0) : 0.f;
+            f[q2][i + 1] = (e + 1 < lim) ? ex2(x1) : 0.f;
+          }
         }
       // ---- dS = P (dP - D), bf16, into the first 32 columns of this half's dP
       got = mbar_wait(bar(2), j & 1, abort_flag);
@@ -429,6 +472,11 @@ __global__ void __launch_bounds__(320, 1)
           }
         }
       }
+    } else if (MASK == kBwdMaskWindow && ok && nkv == 0 && valid) {
+      // no row of this tile sees a key (possible under a window): dQ = 0
+      uint4* const out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dq) + grow * D + h * (D / 2));
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) out[i] = make_uint4(0u, 0u, 0u, 0u);
     }
   }
   tc_fence_before();
@@ -446,7 +494,7 @@ __global__ void __launch_bounds__(320, 1)
 // barriers: 0 kv_full, 1 s_full (S^T), 2 p_done (P^T written), 3 acc_full,
 // 4 drain, 5 dp_full (dP^T), 6 ds_done (dS^T written), then ring
 // full[kRingKV], empty[kRingKV], then the epilogue's staging barrier
-template <int D, bool CAUSAL>
+template <int D, int MASK>
 __global__ void __launch_bounds__(320, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -508,12 +556,27 @@ __global__ void __launch_bounds__(320, 1)
   const int bh = blockIdx.x / p.n_kt;
   const int kt = blockIdx.x % p.n_kt;  // causal: small kt sees the most query tiles
   const int key0 = kt * 128;
-  const int i0 = CAUSAL ? kt : 0;  // first query tile that sees this key tile
-  const int nq = p.n_qt - i0;      // query tiles to visit
+  // query tiles [i0, i0 + nq) see this key tile
+  int i0 = (MASK == kBwdMaskCausal) ? kt : 0;
+  int nq = p.n_qt - i0;
+  if (MASK == kBwdMaskWindow) {
+    // query i keeps key j iff j - diag_off - win_right <= i <= j - diag_off + win_left
+    const long long k_first = key0, k_last = min(key0 + 128, p.Nk) - 1;
+    long long q_lo = 0, q_hi = p.Nq - 1;
+    if (p.win_right >= 0) q_lo = max(0ll, k_first - p.diag_off - p.win_right);
+    if (p.win_left >= 0) q_hi = min(q_hi, k_last - p.diag_off + p.win_left);
+    if (q_lo > q_hi) {
+      nq = 0;  // no query sees a key of this tile: dK = dV = 0
+    } else {
+      i0 = static_cast<int>(q_lo / 128);
+      nq = static_cast<int>(q_hi / 128) + 1 - i0;
+    }
+  }
+  const bool any_q = MASK != kBwdMaskWindow || nq > 0;  // compile-time true without a window
 
   if (warp == 8) {
     // ======================= TMA producer =================================
-    if (lane == 0) {
+    if (lane == 0 && any_q) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
@@ -576,8 +639,8 @@ __global__ void __launch_bounds__(320, 1)
                  C::kIdescAcc, (acc_prev || kk > 0) ? 1u : 0u);
       };
       auto wait_item = [&](int it) -> bool { return mbar_wait(full(item_slot(it)), item_phase(it), abort_flag); };
-      bool ok = mbar_wait(bar(0), 0, abort_flag) && wait_item(0) && wait_item(1);
-      if (ok) {
+      bool ok = !any_q || (mbar_wait(bar(0), 0, abort_flag) && wait_item(0) && wait_item(1));
+      if (ok && any_q) {
         tc_fence_after();
         score(dKd, item_slot(0), kTmS);
         mma_commit(bar(1));
@@ -677,6 +740,17 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t tSh = lane_base + kTmS + h * 64;    // this half's S^T columns (P^T lands in the first 32)
     const uint32_t tDPh = lane_base + kTmDP + h * 64;  // this half's dP^T columns (dS^T likewise)
     const float c = p.scale_log2;
+    // window: queries [key_q_lo, key_q_end) keep this key (bounds clamped into
+    // [-1, Nq], so every later difference fits an int)
+    int key_q_lo = 0, key_q_end = p.Nq;
+    if (MASK == kBwdMaskWindow) {
+      if (p.win_right >= 0)
+        key_q_lo = static_cast<int>(min(static_cast<long long>(p.Nq),
+                                        max(-1ll, static_cast<long long>(key) - p.diag_off - p.win_right)));
+      if (p.win_left >= 0)
+        key_q_end = static_cast<int>(
+            min(static_cast<long long>(p.Nq), max(-1ll, static_cast<long long>(key) - p.diag_off + p.win_left) + 1));
+    }
     bool ok = true;
     for (int ii = 0; ii < nq; ++ii) {
       const int i = i0 + ii;
@@ -698,8 +772,12 @@ __global__ void __launch_bounds__(320, 1)
       tmem_ld_wait(s0);
       reg_pin(s1);
       float* const f[2] = {reinterpret_cast<float*>(s0), reinterpret_cast<float*>(s1)};
-      // causal: query q sees this key iff q >= key; only the diagonal tile masks
-      const int qlim = (CAUSAL && i == kt) ? key_local - h * 64 : 0;  // this half's columns < qlim are masked
+      // causal: query q sees this key iff q >= key; only the diagonal tile masks;
+      // window: this half's columns [qlo, qend) are kept
+      const int qlim = (MASK == kBwdMaskCausal && i == kt) ? key_local - h * 64 : 0;  // columns < qlim are masked
+      const int qcol0 = i * 128 + h * 64;
+      const int qlo = (MASK == kBwdMaskWindow) ? key_q_lo - qcol0 : 0;
+      const int qend = (MASK == kBwdMaskWindow) ? key_q_end - qcol0 : 64;
       // P^T = 2^(S^T c - L[q]); padding queries have L = +inf, so P^T = 0 there
 #pragma unroll
       for (int q2 = 0; q2 < 2; ++q2) {
@@ -712,7 +790,10 @@ __global__ void __launch_bounds__(320, 1)
           for (int t = 0; t < 4; ++t) {
             const int col = q2 * 32 + i4 * 4 + t;
             const float x = fmaf(f[q2][i4 * 4 + t], c, -lv[t]);
-            f[q2][i4 * 4 + t] = (col >= qlim) ? ex2(x) : 0.f;
+            if (MASK == kBwdMaskWindow)
+              f[q2][i4 * 4 + t] = (col >= qlo && col < qend) ? ex2(x) : 0.f;
+            else
+              f[q2][i4 * 4 + t] = (col >= qlim) ? ex2(x) : 0.f;
           }
         }
 #pragma unroll
@@ -808,6 +889,16 @@ __global__ void __launch_bounds__(320, 1)
             report_wait_failure(abort_flag, 8u);
           }
         }
+      }
+    } else if (MASK == kBwdMaskWindow && ok && nq == 0 && key < p.Nk) {
+      // no query sees a key of this tile (possible under a window): dK = dV = 0
+      const size_t grow = static_cast<size_t>(bh) * p.Nk + key;
+      uint4* const outv = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dv) + grow * D + h * (D / 2));
+      uint4* const outk = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dk) + grow * D + h * (D / 2));
+#pragma unroll
+      for (int i = 0; i < D / 16; ++i) {
+        outv[i] = make_uint4(0u, 0u, 0u, 0u);
+        outk[i] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
   }

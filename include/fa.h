@@ -156,7 +156,22 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int causal,
            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Workspace bytes fa_bwd needs (0 for invalid sizes). */
+/*
+ * fa_bwd_window -- fa_bwd under the sliding-window mask of fa_fwd_window (key j
+ * kept for query row i iff i + (Nk - Nq) - window_left <= j <= i + (Nk - Nq) +
+ * window_right; -1 leaves that side open, so (-1, 0) is the causal mask aligned
+ * bottom-right, for any Nq and Nk).  o and lse must come from fa_fwd_window
+ * with the same window: a row that keeps no key has lse = -inf and o = 0 there,
+ * and its dQ is written as 0; a key that no row keeps gets dK = dV = 0.
+ * Each kernel visits only the tiles its window reaches.
+ * Arguments, workspace and errors as fa_bwd (no causal argument); a bound
+ * below -1 is FA_ERR_SHAPE.
+ */
+int fa_bwd_window(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                  void* dq, void* dk, void* dv, int B, int H, int Nq, int Nk, int d, float scale, int window_left,
+                  int window_right, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes fa_bwd and fa_bwd_window need (0 for invalid sizes). */
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq);
 
 /* Size of the fixed device array fa_fwd_splitkv_noalloc works in. */

@@ -127,6 +127,96 @@ def test_bwd_outputs_not_written_outside(d, shape):
         assert _err(g, r) <= TOL, f"{name} normwise error {_err(g, r):.3e}"
 
 
+# --- sliding window (fa_bwd_window) ------------------------------------------
+# (B, H, Nq, Nk, window): a band, a symmetric window, the causal mask aligned
+# bottom-right for Nq != Nk, Nq > Nk with rows (whole query tiles) that keep no
+# key, Nq < Nk with key tiles no row keeps, the diagonal alone, an open window
+# (no mask) and a one-tile-wide band over ragged tiles
+WINDOW_CASES = [
+    (1, 2, 1000, 1000, (100, 0)),
+    (1, 2, 1000, 1000, (64, 64)),
+    (2, 1, 300, 1000, (-1, 0)),
+    (1, 2, 640, 200, (0, 1)),
+    (1, 2, 200, 640, (0, 0)),
+    (1, 1, 461, 77, (5, 5)),
+    (1, 2, 333, 333, (0, 0)),
+    (1, 1, 257, 129, (-1, -1)),
+    (2, 2, 129, 1000, (127, 1)),
+]
+
+
+def _window_grads(q, k, v, do, scale, window, guard=0):
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    tq, tk, tv, tdo = (to_device(x) for x in (q, k, v, do))
+    o, lse = fa.fwd(tq, tk, tv, scale=scale, window=window)
+    bufs, outs = [], []
+    for like in (tq, tk, tv):
+        big = torch.full((like.numel() + 2 * guard,), 7.0, dtype=torch.bfloat16, device="cuda")
+        bufs.append(big)
+        outs.append(big[guard:guard + like.numel()].view(like.shape))
+    fa.bwd(tq, tk, tv, o, lse, tdo, scale=scale, window=window, dq=outs[0], dk=outs[1], dv=outs[2])
+    torch.cuda.synchronize()
+    st, word = fa.fa_fwd_status(None, clear=True)
+    assert st == 0, f"kernel wait timed out, status word {word:#x}"
+    for big, t in zip(bufs, outs):
+        assert torch.all(big[:guard] == 7.0) and torch.all(big[guard + t.numel():] == 7.0)
+    return tuple(t.float().cpu().numpy().astype(np.float64) for t in outs)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=[f"{c[2]}x{c[3]}_w{c[4][0]}_{c[4][1]}" for c in WINDOW_CASES])
+def test_bwd_window(d, case):
+    B, H, nq, nk, window = case
+    w = synth.Workload("bwd_window", B, H, nq, nk, d, False, seed=31 + nq + nk)
+    q, k, v = w.make()
+    do = synth.normal_bf16(w.seed + 7, 3, w.q_shape())
+    got = _window_grads(q, k, v, do, w.scale, window, guard=2048)
+    ref = backward.attention_bwd(q, k, v, do, w.scale, window=window)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert np.all(np.isfinite(g)), f"{name} not finite"
+        assert _err(g, r) <= TOL, f"{name} normwise error {_err(g, r):.3e}"
+    # rows that keep no key and keys no row keeps (keep-matrix by enumeration)
+    # have gradients of exactly zero
+    wl, wr = window
+    off = np.arange(nk)[None, :] - (np.arange(nq)[:, None] + nk - nq)
+    keep = ((wl < 0) | (off >= -wl)) & ((wr < 0) | (off <= wr))
+    dead_rows, dead_keys = ~keep.any(axis=1), ~keep.any(axis=0)
+    assert np.all(got[0][:, :, dead_rows] == 0.0)
+    assert np.all(got[1][:, :, dead_keys] == 0.0) and np.all(got[2][:, :, dead_keys] == 0.0)
+    if window == (0, 1) or window == (0, 0) and nq != nk:
+        assert dead_rows.any() or dead_keys.any()  # the empty-tile paths are exercised
+
+
+def test_bwd_window_bottom_right_causal_matches_causal():
+    """(-1, 0) with Nq == Nk is the causal mask: same gradients as fa_bwd(causal)."""
+    w = synth.Workload("bwd_wc", 2, 2, 700, 700, 128, True, seed=37)
+    q, k, v = w.make()
+    do = synth.normal_bf16(w.seed + 7, 3, w.q_shape())
+    got_w = _window_grads(q, k, v, do, w.scale, (-1, 0))
+    got_c = _gpu_grads(q, k, v, do, w.scale, True)
+    for a, b in zip(got_w, got_c):
+        assert np.array_equal(a, b)
+
+
+def test_bwd_window_errors():
+    import torch
+
+    import exact_attention_19_gb300 as fa
+
+    q = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((1, 1, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(1, 1, 128), dtype=torch.uint8, device="cuda")
+    args = [q.data_ptr()] * 3 + [q.data_ptr(), lse.data_ptr(), q.data_ptr()]
+    outs = [torch.empty_like(q).data_ptr() for _ in range(3)]
+    st = fa.fa_bwd_window(*args, *outs, 1, 1, 128, 128, 64, 0.125, -2, 0, ws.data_ptr(), ws.numel(), None)
+    assert st == 3  # FA_ERR_SHAPE: a bound below -1
+    st = fa.fa_bwd_window(*args, *outs, 1, 1, 128, 128, 64, 0.125, 4, 4, ws.data_ptr(), 16, None)
+    assert st == 11  # FA_ERR_WORKSPACE
+
+
 def test_bwd_deterministic():
     w = synth.Workload("bwd_det", 1, 3, 700, 700, 128, True, seed=830)
     q, k, v = w.make()
