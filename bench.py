@@ -151,8 +151,30 @@ def load_peaks():
 
 
 def visible_keys(w: synth.Workload, rows: np.ndarray) -> np.ndarray:
+    """Keys each flat query row attends to: all Nk, i + 1 under the causal mask,
+    or the keys its sliding window keeps (bottom-right alignment, -1 = open side)."""
     i = rows % w.Nq
+    if w.window is not None:
+        wl, wr = w.window
+        s = w.Nk - w.Nq
+        lo = np.maximum(0, i + s - wl) if wl >= 0 else np.zeros_like(i)
+        hi = np.minimum(w.Nk, i + s + wr + 1) if wr >= 0 else np.full(i.shape, w.Nk)
+        return np.maximum(0, hi - lo)
     return np.minimum(i + 1, w.Nk) if w.causal else np.full(rows.shape, w.Nk)
+
+
+def flops_of(w: synth.Workload) -> float:
+    """Counted forward FLOPs: 4*B*H*Nq*Nk*d, halved under the causal mask (the
+    metric's convention); under a window, 4*d per (row, key) pair it keeps."""
+    if w.window is None:
+        return w.flops
+    kept = float(np.sum(visible_keys(w, np.arange(w.Nq))))
+    return 4.0 * w.B * w.H * kept * w.d
+
+
+def pairs_of(w: synth.Workload) -> float:
+    """(row, key) pairs whose exponential is taken per step."""
+    return flops_of(w) / (4.0 * w.d)
 
 
 def sample_rows_even(w: synth.Workload, n: int) -> np.ndarray:
@@ -247,11 +269,11 @@ def time_oracle(w: synth.Workload, q, k, v, budget_s: float, max_rows: int | Non
     # calibrate: a warm-up call (thread pool, page faults), then grow the
     # sample until one call takes a measurable fraction of the budget
     n_probe = 16
-    oracle.attention_rows(q, k, v, sample_rows_even(w, n_probe), w.scale, w.causal)
+    oracle.attention_rows(q, k, v, sample_rows_even(w, n_probe), w.scale, w.causal, window=w.window)
     while True:
         probe = sample_rows_even(w, n_probe)
         t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, probe, w.scale, w.causal)
+        oracle.attention_rows(q, k, v, probe, w.scale, w.causal, window=w.window)
         t_probe = max(time.perf_counter() - t0, 1e-6)
         if t_probe >= 0.05 * budget_s or probe.size >= w.B * w.H * w.Nq:
             break
@@ -261,7 +283,7 @@ def time_oracle(w: synth.Workload, q, k, v, budget_s: float, max_rows: int | Non
         n = min(n, max_rows)
     rows = sample_rows_even(w, max(n, 16))
     t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, rows, w.scale, w.causal)
+    oracle.attention_rows(q, k, v, rows, w.scale, w.causal, window=w.window)
     secs = time.perf_counter() - t0
     flops = float(np.sum(4.0 * visible_keys(w, rows) * w.d))
     return flops / secs / 1e12, secs, int(rows.size), oracle.threads()
@@ -302,7 +324,9 @@ def run_reference(args, w: synth.Workload, rank: int):
 def config_of(w: synth.Workload, l2_note: str | None = None):
     c = {"workload": w.name, "B": w.B, "H": w.H, "Nq": w.Nq, "Nk": w.Nk, "d": w.d, "causal": w.causal,
          "scale": w.scale, "inputs": f"bf16 q~N(0,{w.sigma_q:g}^2), k,v~N(0,1), seed {w.seed}",
-         "flops_per_step": w.flops}
+         "flops_per_step": flops_of(w)}
+    if w.window is not None:
+        c["window"] = list(w.window)
     if l2_note:
         c["l2"] = l2_note
     return c
@@ -353,8 +377,8 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     launches_per_step = 2 if n_splits > 1 else 1
 
     def step():
-        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, n_splits=n_splits,
-               workspace=workspace)
+        fa.fwd(q, k, v, causal=w.causal, scale=w.scale, window=w.window, out=o, lse=lse, stream=stream,
+               n_splits=n_splits, workspace=workspace)
 
     def barrier():
         if dist is not None:
@@ -411,8 +435,8 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
             qd.copy_(q_p, non_blocking=True)
             kd.copy_(k_p, non_blocking=True)
             vd.copy_(v_p, non_blocking=True)
-            fa.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, out=o, lse=lse, stream=stream, n_splits=n_splits,
-                   workspace=workspace)
+            fa.fwd(qd, kd, vd, causal=w.causal, scale=w.scale, window=w.window, out=o, lse=lse, stream=stream,
+                   n_splits=n_splits, workspace=workspace)
             o_host[0].copy_(o, non_blocking=True)
             lse_host[0].copy_(lse, non_blocking=True)
 
@@ -438,7 +462,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
                 stream.wait_event(ev_in[b])
                 if i >= 2:
                     stream.wait_event(ev_out[b])  # step i-2's outputs have been read back
-                fa.fwd(qb, kb, vb, causal=w.causal, scale=w.scale, out=ob, lse=lb, stream=stream,
+                fa.fwd(qb, kb, vb, causal=w.causal, scale=w.scale, window=w.window, out=ob, lse=lb, stream=stream,
                        n_splits=n_splits, workspace=workspace)
                 ev_kernel[b].record(stream)
                 d2h_stream.wait_event(ev_kernel[b])
@@ -472,9 +496,9 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     # ---- max over ranks -------------------------------------------------------
     t_max_elapsed, t_max_e2e, t_max_e2e_serial = max_over_ranks([elapsed, e2e_ms, e2e_serial_ms], dist, dev)
     times = [t_max_elapsed] * world
-    value, t_max = aggregate(times, [w.flops * args.steps] * world)
-    e2e_value, _ = aggregate([t_max_e2e] * world, [w.flops] * world)
-    e2e_serial_value, _ = aggregate([t_max_e2e_serial] * world, [w.flops] * world)
+    value, t_max = aggregate(times, [flops_of(w) * args.steps] * world)
+    e2e_value, _ = aggregate([t_max_e2e] * world, [flops_of(w)] * world)
+    e2e_serial_value, _ = aggregate([t_max_e2e_serial] * world, [flops_of(w)] * world)
     ms_per_step = t_max / args.steps
 
     if rank != 0:
@@ -483,11 +507,11 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     peaks, peaks_kind = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    achieved = w.flops / (ms_per_step * 1e-3) / 1e12
+    achieved = flops_of(w) / (ms_per_step * 1e-3) / 1e12
     achieved_gbs = w.algorithmic_bytes / (ms_per_step * 1e-3) / 1e9
     src_hash = kernel_source_hash()
     traffic = read_traffic(w.name, src_hash)
-    roofline = roofline_entry(w.flops, w.algorithmic_bytes, achieved, achieved_gbs, peak, hbm)
+    roofline = roofline_entry(flops_of(w), w.algorithmic_bytes, achieved, achieved_gbs, peak, hbm)
     roofline.update({"traffic": traffic, "peak_kind": f"{roofline['peak_kind']}, {peaks_kind}",
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                      "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
@@ -496,7 +520,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
 
     # third roofline: exponentials (one ex2 per visible score) per SM clock
     # against the probe's rate, at the median SM clock seen under load
-    ex2_per_step = w.B * w.H * w.Nq * w.Nk / (2 if w.causal else 1)
+    ex2_per_step = pairs_of(w)
     mufu = None
     if clocks.get("sm_mhz"):
         rate = ex2_per_step / (ms_per_step * 1e-3) / (float(clocks["sm_mhz"]) * 1e6) / n_sm
@@ -555,7 +579,7 @@ def run_bwd(args, w: synth.Workload, local_rank: int):
         return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
 
     q, k, v, do = up(q_h), up(k_h), up(v_h), up(do_h)
-    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale, n_splits=1)
+    o, lse = fa.fwd(q, k, v, causal=w.causal, scale=w.scale, window=w.window, n_splits=1)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(fa.fa_bwd_workspace_bytes(w.B, w.H, w.Nq), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -567,8 +591,8 @@ def run_bwd(args, w: synth.Workload, local_rank: int):
                else f"L2 flushed between timed steps ({2 * L2_BYTES / 1e6:.0f} MB write)")
 
     def step():
-        fa.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, dq=dq, dk=dk, dv=dv, workspace=ws,
-               stream=stream)
+        fa.bwd(q, k, v, o, lse, do, causal=w.causal, scale=w.scale, window=w.window, dq=dq, dk=dk, dv=dv,
+               workspace=ws, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -592,7 +616,7 @@ def run_bwd(args, w: synth.Workload, local_rank: int):
     if st != 0:
         raise RuntimeError(f"kernel reported a wait timeout (status {word:#x})")
     ms = elapsed / args.steps
-    flops = 2.5 * w.flops
+    flops = 2.5 * flops_of(w)
     peaks, kind = load_peaks()
     value = flops / (ms * 1e-3) / 1e12
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -624,10 +648,21 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--pass", dest="which", choices=["fwd", "bwd"], default="fwd",
                     help="bwd: time fa_bwd instead (FLOPs counted as 2.5x the forward's)")
+    ap.add_argument("--window", default=None, metavar="LEFT,RIGHT",
+                    help="sliding-window mask over the workload (bottom-right, -1 = open side); "
+                         "FLOPs then count 4*d per kept (row, key) pair")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = synth.WORKLOADS[args.workload]
+    if args.window is not None:
+        try:
+            wl, wr = (int(x) for x in args.window.split(","))
+        except ValueError:
+            ap.error("--window takes two integers: LEFT,RIGHT")
+        if wl < -1 or wr < -1:
+            ap.error("--window bounds must be >= -1")
+        w = w.with_(window=(wl, wr), causal=False)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -135,6 +135,7 @@ class Workload:
     sigma_k: float = 1.0
     sigma_v: float = 1.0
     seed: int = 1000
+    window: tuple | None = None  # (left, right) sliding-window bounds, -1 = open; None: no window
 
     @property
     def scale(self) -> float:

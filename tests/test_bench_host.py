@@ -28,6 +28,29 @@ def test_visible_keys_and_sampling():
     assert r[0] == 0 and r[-1] == 19 and len(set(r)) == len(r)
 
 
+def test_window_flops_closed_forms():
+    """Kept (row, key) pairs under a window, against closed forms: the causal
+    triangle, the diagonal alone, a band, an open window, and Nq > Nk rows that
+    keep nothing."""
+    base = synth.Workload("w", 2, 3, 100, 100, 64, False)
+    per_pair = 4.0 * 2 * 3 * 64
+    assert bench.flops_of(base.with_(window=(-1, 0))) == per_pair * 100 * 101 / 2
+    assert bench.flops_of(base.with_(window=(0, 0))) == per_pair * 100
+    # band of 10 keys back: row i keeps min(i, 10) + 1 keys
+    assert bench.flops_of(base.with_(window=(10, 0))) == per_pair * (sum(range(1, 11)) + 90 * 11)
+    assert bench.flops_of(base.with_(window=(-1, -1))) == base.flops
+    assert bench.flops_of(base.with_(window=(500, 500))) == base.flops
+    # Nq = 100 > Nk = 30, diagonal window: only the last 30 rows keep a key (one each)
+    tall = synth.Workload("t", 1, 1, 100, 30, 64, False, window=(0, 0))
+    assert bench.flops_of(tall) == 4.0 * 64 * 30
+    assert bench.pairs_of(tall) == 30
+    keys = bench.visible_keys(tall, np.arange(100))
+    assert np.all(keys[:70] == 0) and np.all(keys[70:] == 1)
+    # no window: the metric's convention, halved under the causal mask
+    assert bench.flops_of(base) == base.flops
+    assert bench.flops_of(base.with_(causal=True)) == base.flops / 2
+
+
 def test_traffic_lookup(tmp_path, monkeypatch):
     h = bench.kernel_source_hash()
     f = tmp_path / "traffic.md"
