@@ -111,6 +111,22 @@ def test_reference_arm_line(monkeypatch):
     assert line["config"]["workload"] == "single_head_256_d64"
 
 
+def test_reference_arm_window_line(monkeypatch):
+    """--window reaches the oracle leg: the line names the window and counts the
+    kept pairs (a 16-key band over 256 rows: 16*17/2 + 240*17 pairs)."""
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--steps", "1", "--warmup", "3", "--workload",
+                         "single_head_256_d64", "--window", "16,0"])
+    assert rc == 0
+    line = json.loads(buf.getvalue().strip().splitlines()[-1])
+    assert line["config"]["window"] == [16, 0] and line["config"]["causal"] is False
+    assert line["config"]["flops_per_step"] == 4.0 * 64 * (16 * 17 / 2 + 240 * 17)
+    assert line["value"] > 0
+
+
 def test_reference_arm_other_ranks_silent(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
