@@ -53,7 +53,8 @@ struct BwdParams {
 };
 
 // kBwdMaskCausal: key j kept for row i iff j <= i (Nq == Nk); kBwdMaskWindow:
-// the general window of BwdParams.  Each kernel then visits only the tiles its
+// the general window of BwdParams (the forward's reading of the "sliding" mask
+// named in page "llm-infra-atlas / FlashAttention 01", section 3).  Each kernel then visits only the tiles its
 // rows (keys) can see; a tile that sees none writes zero gradients.
 enum : int { kBwdMaskNone = 0, kBwdMaskCausal = 1, kBwdMaskWindow = 2 };
 
