@@ -143,3 +143,18 @@ def test_bwd_host_validation(lib):
     assert fa.fa_bwd(*args, 1, 1, 0, 128, 64, 0.125, 0, FAKE, 1 << 20, None) == 3
     assert fa.fa_bwd(*args, 1, 1, 128, 128, 64, 0.125, 0, FAKE, 16, None) == 11
     assert fa.fa_bwd_workspace_bytes(2, 3, 200) == 2 * 6 * 256 * 4
+
+
+def test_bwd_window_host_validation(lib):
+    args = [FAKE] * 9
+    assert fa.fa_bwd_window(*args, 1, 1, 128, 128, 64, 0.125, -2, 0, FAKE, 1 << 20, None) == 3
+    assert fa.fa_bwd_window(*args, 1, 1, 128, 128, 64, 0.125, 0, -7, FAKE, 1 << 20, None) == 3
+    assert fa.fa_bwd_window(None, *args[1:], 1, 1, 128, 128, 64, 0.125, 4, 0, FAKE, 1 << 20, None) == 1
+    assert fa.fa_bwd_window(*args, 1, 1, 128, 128, 64, 0.125, 4, 0, None, 1 << 20, None) == 1
+    assert fa.fa_bwd_window(*args, 1, 1, 128, 128, 96, 0.125, 4, 0, FAKE, 1 << 20, None) == 4
+    assert fa.fa_bwd_window(*args, 1, 1, 0, 128, 64, 0.125, 4, 0, FAKE, 1 << 20, None) == 3
+    assert fa.fa_bwd_window(*args, 1, 1, 128, 128, 64, float("nan"), 4, 0, FAKE, 1 << 20, None) == 9
+    assert fa.fa_bwd_window(*args, 1, 1, 128, 128, 64, 0.125, 4, 0, FAKE, 16, None) == 11
+    # a window needs no Nq == Nk: (-1, 0) with Nq != Nk passes every shape check
+    st = fa.fa_bwd_window(*args, 1, 1, 128, 256, 64, 0.125, -1, 0, FAKE, 1 << 20, None)
+    assert st not in (3, 5)
