@@ -41,6 +41,33 @@ def test_library_exports_every_declared_symbol(lib):
         assert getattr(lib, name) is not None
 
 
+def test_plain_c_consumer(lib, tmp_path):
+    """include/fa.h is plain C: a C11 program compiled with -pedantic -Werror links
+    libfa_gb300.so and gets the version, a message and a host-side argument error
+    (no device work, so no GPU is needed)."""
+    import shutil
+
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "include")
+    src = tmp_path / "consumer.c"
+    src.write_text(
+        "#include <stdio.h>\n#include \"fa.h\"\n"
+        "int main(void) {\n"
+        "  printf(\"%d|%s|\", fa_version(), fa_strerror(FA_ERR_HEADDIM));\n"
+        "  printf(\"%d\\n\", fa_fwd(NULL, NULL, NULL, NULL, NULL, 1, 1, 128, 128, 96, 0.125f, 0, (cudaStream_t)0));\n"
+        "  return 0;\n}\n")
+    exe = tmp_path / "consumer"
+    lib_dir = os.path.dirname(fa.library_path())
+    subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.dirname(HEADER),
+                    "-I", cuda_inc, str(src), "-L", lib_dir, "-lfa_gb300", f"-Wl,-rpath,{lib_dir}", "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.strip()
+    version, message, status = out.split("|")
+    assert int(version) == lib.fa_version()
+    assert message == lib.fa_strerror(4).decode()
+    assert int(status) == 1  # FA_ERR_NULL: null pointers are reported first
+
+
 def test_version_and_strerror(lib):
     assert fa.fa_version() == 100
     assert fa.fa_strerror(0) == "ok"
