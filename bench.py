@@ -654,6 +654,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.impl == "reference" and args.which == "bwd":
+        ap.error("the reference arm times the forward oracle only; --pass bwd has none")
     w = synth.WORKLOADS[args.workload]
     if args.window is not None:
         try:

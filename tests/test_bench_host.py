@@ -127,6 +127,12 @@ def test_reference_arm_window_line(monkeypatch):
     assert line["value"] > 0
 
 
+def test_reference_arm_rejects_backward():
+    with pytest.raises(SystemExit) as e:
+        bench.main(["--impl", "reference", "--pass", "bwd"])
+    assert e.value.code == 2
+
+
 def test_reference_arm_other_ranks_silent(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
