@@ -174,11 +174,11 @@ int launch_bwd(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& 
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-// Checks shared by fa_fwd and fa_fwd_splitkv.  On success fills the tensor
-// maps and the common parameters; *noop is set when Nq == 0.
-int prepare_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                 int d, float scale, int causal, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
-                 CUtensorMap* mo, fa::FwdParams* p, int* dev_out, bool* noop) {
+// Host-only checks shared by fa_fwd, fa_fwd_window and both split-KV entry
+// points, in the order fa.h documents; nothing here touches the device.
+// *noop is set when Nq == 0 (nothing is read or written).
+int check_args(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+               int d, float scale, int causal, bool* noop) {
   *noop = false;
   // With Nq == 0 nothing is read or written, so the (empty) tensors may be NULL.
   if ((Nq != 0 && (!q || !o || !lse)) || !k || !v) return FA_ERR_NULL;
@@ -196,10 +196,17 @@ int prepare_call(const void* q, const void* k, const void* v, void* o, float* ls
   // tensor-map limits: a stride below 2^40 bytes, grid below 2^31 CTAs
   if (static_cast<long long>(Nq > Nk ? Nq : Nk) * d * 2 >= (1ll << 40)) return FA_ERR_SHAPE;
   if (BH >= (1ll << 31) || BH * n_pairs >= (1ll << 31)) return FA_ERR_SHAPE;
-  if (Nq == 0) {
-    *noop = true;
-    return FA_OK;
-  }
+  if (Nq == 0) *noop = true;
+  return FA_OK;
+}
+
+// The device side of a forward call whose arguments passed check_args (with
+// Nq > 0): the current device, its one-time set-up, the pointer checks, the
+// TMA tensor maps and the parameters common to every forward kernel.
+int prepare_launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                   int d, float scale, int causal, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
+                   CUtensorMap* mo, fa::FwdParams* p, int* dev_out) {
+  const long long BH = static_cast<long long>(B) * H;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
   const int prep = prepare_device(dev);
@@ -214,7 +221,7 @@ int prepare_call(const void* q, const void* k, const void* v, void* o, float* ls
   p->lse = lse;
   p->Nq = Nq;
   p->Nk = Nk;
-  p->n_pairs = static_cast<int>(n_pairs);
+  p->n_pairs = static_cast<int>((static_cast<long long>(Nq) + 255) / 256);
   p->scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634074);
   // causal = the window (-1, 0) on the main diagonal (Nq == Nk here)
   p->win_left = -1;
@@ -235,12 +242,36 @@ int prepare_call(const void* q, const void* k, const void* v, void* o, float* ls
   return FA_OK;
 }
 
+// check_args then prepare_launch; *noop is set (and nothing else done) when Nq == 0.
+int prepare_call(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                 int d, float scale, int causal, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv,
+                 CUtensorMap* mo, fa::FwdParams* p, int* dev_out, bool* noop) {
+  const int st = check_args(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, noop);
+  if (st != FA_OK || *noop) return st;
+  return prepare_launch(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, mq, mk, mv, mo, p, dev_out);
+}
+
 // K/V tiles per split and the number of non-empty splits for a request.
 void split_shape(int Nk, int n_splits, int* split_tiles, int* eff_splits) {
   const int n_kv = (Nk + 127) / 128;
   const int req = n_splits < 1 ? 1 : (n_splits > n_kv ? n_kv : n_splits);
   *split_tiles = (n_kv + req - 1) / req;
   *eff_splits = (n_kv + *split_tiles - 1) / *split_tiles;
+}
+
+// Single-pass forward (no mask or causal) on prepared maps and parameters.
+int launch_single_pass(int B, int H, int Nq, int Nk, int d, int causal, const CUtensorMap& mq,
+                       const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, fa::FwdParams p,
+                       cudaStream_t stream) {
+  if (d == 64 && causal && Nk <= kSingleTileMaxKeys) {
+    p.n_pairs = (Nq + 127) / 128;  // one query tile per CTA
+    const long long grid = static_cast<long long>(B) * H * p.n_pairs;
+    if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
+    return launch<64, fa::kMaskCausal, false, 1>(mq, mk, mv, mo, p, grid, stream);
+  }
+  const long long grid = static_cast<long long>(B) * H * p.n_pairs;
+  return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, mo, p, grid, stream)
+                 : launch_d<128, false>(causal, mq, mk, mv, mo, p, grid, stream);
 }
 
 }  // namespace
@@ -275,15 +306,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   bool noop = false;
   const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &mo, &p, &dev, &noop);
   if (st != FA_OK || noop) return st;
-  if (d == 64 && causal && Nk <= kSingleTileMaxKeys) {
-    p.n_pairs = (Nq + 127) / 128;  // one query tile per CTA
-    const long long grid = static_cast<long long>(B) * H * p.n_pairs;
-    if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
-    return launch<64, fa::kMaskCausal, false, 1>(mq, mk, mv, mo, p, grid, stream);
-  }
-  const long long grid = static_cast<long long>(B) * H * p.n_pairs;
-  return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, mo, p, grid, stream)
-                 : launch_d<128, false>(causal, mq, mk, mv, mo, p, grid, stream);
+  return launch_single_pass(B, H, Nq, Nk, d, causal, mq, mk, mv, mo, p, stream);
 }
 
 int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
@@ -331,24 +354,73 @@ int fa_splitkv_heuristic(int B, int H, int Nq, int Nk, int d, int causal) {
   return eff;
 }
 
-int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
-                   int d, float scale, int causal, int n_splits, void* workspace, size_t workspace_bytes,
-                   cudaStream_t stream) {
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free split-KV: the slice buffers of fa_fwd_splitkv_noalloc.  For
+// callers that may not allocate device memory themselves (a host framework
+// that owns the whole device pool, or a latency path where a cudaMalloc and
+// its implicit synchronisation are not allowed), they live in one fixed array
+// in the library's own device memory.  Each GPU that loads the library holds
+// this array until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::atomic<void*> g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
+std::mutex g_noalloc_mutex;
+
+// The host-side name of a __device__ array is only a stand-in; the address a
+// kernel may use is asked of the runtime once per device, with that device
+// current, and cached (later calls take the lock-free path).
+void* noalloc_scratch(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* ptr = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (ptr) return ptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  ptr = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (!ptr) {
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_noalloc_ptr[dev].store(ptr, std::memory_order_release);
+  }
+  return ptr;
+}
+
+// Both split-KV entry points.  Checks run in one order for both: the host
+// checks of fa_fwd (and the Nq == 0 no-op), then, for the allocation-free
+// call, the size limit of the fixed array, then the device and pointer checks,
+// and only then the workspace: the caller's, or the fixed array's address.
+int splitkv_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                 int d, float scale, int causal, int n_splits, void* workspace, size_t workspace_bytes,
+                 bool noalloc, cudaStream_t stream) {
   if (n_splits < 1 || n_splits > 64) return FA_ERR_SHAPE;
-  CUtensorMap mq, mk, mv, mo;
-  fa::FwdParams p;
-  int dev = -1;
   bool noop = false;
-  const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &mo, &p, &dev, &noop);
+  int st = check_args(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &noop);
   if (st != FA_OK || noop) return st;
   int tiles = 0, eff = 0;
   split_shape(Nk, n_splits, &tiles, &eff);
-  if (eff == 1)  // one slice: the plain kernel, no workspace needed
-    return fa_fwd(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, stream);
-  const size_t need = fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits);
-  if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
-  if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
-  if (!is_device_pointer(workspace, dev)) return FA_ERR_POINTER;
+  // one slice runs the plain kernel and needs no workspace
+  const size_t need = eff > 1 ? fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits) : 0;
+  if (noalloc && need > FA_NOALLOC_SCRATCH_BYTES) return FA_ERR_WORKSPACE;
+  CUtensorMap mq, mk, mv, mo;
+  fa::FwdParams p;
+  int dev = -1;
+  st = prepare_launch(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &mo, &p, &dev);
+  if (st != FA_OK) return st;
+  if (eff == 1) return launch_single_pass(B, H, Nq, Nk, d, causal, mq, mk, mv, mo, p, stream);
+  if (noalloc) {
+    // Every partial the merge reads is written earlier in the same call (an
+    // empty slice writes weight 2^-inf), so nothing in the array is cleared.
+    workspace = noalloc_scratch(dev);
+    if (!workspace) return FA_ERR_LAUNCH;
+  } else {
+    if (!workspace || workspace_bytes < need) return FA_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 15u) return FA_ERR_ALIGN;
+    if (!is_device_pointer(workspace, dev)) return FA_ERR_POINTER;
+  }
   p.n_splits = eff;
   p.split_tiles = tiles;
   p.o_part = static_cast<float*>(workspace);
@@ -392,52 +464,20 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                             : cudaLaunchKernelEx(&cfg, fa::fa_splitkv_combine_kernel<128>, o_part, lse_part, o, lse, rows, eff);
   return (e == cudaSuccess && cudaGetLastError() == cudaSuccess) ? FA_OK : FA_ERR_LAUNCH;
 }
-
-// ---------------------------------------------------------------------------
-// Allocation-free split-KV.  For callers that may not allocate device memory
-// themselves (a host framework that owns the whole device pool, or a latency
-// path where a cudaMalloc and its implicit synchronisation are not allowed),
-// the slice buffers live in one fixed array in the library's own device
-// memory.  Each GPU that loads the library holds this array until the
-// process exits.
-// ---------------------------------------------------------------------------
-static __device__ __align__(256) unsigned char g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES];
-
-namespace {
-void* g_noalloc_ptr[kMaxDevices];  // device address of g_noalloc_scratch, per device
-std::mutex g_noalloc_mutex;
-
-// The host-side name of a __device__ array is only a stand-in; the address a
-// kernel may use is asked of the runtime once per device, with that device
-// current.
-void* noalloc_scratch(int dev) {
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) {
-      cudaGetLastError();
-      return nullptr;
-    }
-    g_noalloc_ptr[dev] = ptr;
-  }
-  return g_noalloc_ptr[dev];
-}
 }  // namespace
+
+extern "C" {
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq, int Nk,
+                   int d, float scale, int causal, int n_splits, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
+  return splitkv_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, workspace, workspace_bytes, false,
+                      stream);
+}
 
 int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
                            int Nk, int d, float scale, int causal, int n_splits, cudaStream_t stream) {
-  if (n_splits < 1 || n_splits > 64) return FA_ERR_SHAPE;
-  if (Nq > 0 && fa_splitkv_workspace_bytes(B, H, Nq, Nk, d, n_splits) > FA_NOALLOC_SCRATCH_BYTES)
-    return FA_ERR_WORKSPACE;
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_LAUNCH;
-  void* scratch = noalloc_scratch(dev);
-  if (!scratch) return FA_ERR_LAUNCH;
-  // Every partial the merge reads is written earlier in the same call (an
-  // empty slice writes weight 2^-inf), so nothing in the array has to be cleared.
-  return fa_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, scratch,
-                        FA_NOALLOC_SCRATCH_BYTES, stream);
+  return splitkv_impl(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, n_splits, nullptr, 0, true, stream);
 }
 
 // ---------------------------------------------------------------------------

@@ -16,6 +16,12 @@
  *
  * All functions have C linkage, never throw, never print and never abort the
  * process.  None of them allocates device memory.
+ *
+ * The first call on a device records per-device state in the library (the
+ * kernels' shared-memory opt-in, the multiprocessor count and L2 size, and
+ * for fa_fwd_splitkv_noalloc the device address of its fixed array).
+ * Resetting a device (cudaDeviceReset) after this library has used it is not
+ * supported: that state would be stale.
  */
 #ifndef FA_GB300_H
 #define FA_GB300_H

@@ -153,6 +153,36 @@ def test_noalloc_host_validation(lib):
     assert st == 11
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), 1), (dict(lse=None), 1), (dict(k=FAKE + 2), 2), (dict(d=96), 4), (dict(B=0), 3),
+    (dict(causal=1, Nk=256), 5), (dict(scale=float("nan")), 9), (dict(Nq=0), 0),
+    (dict(Nq=0, q=None, o=None, lse=None), 0),
+    # oversized for the fixed array, but an argument error comes first
+    (dict(q=None, H=64, Nq=4096, Nk=4096, d=128), 1), (dict(d=96, H=64, Nq=4096, Nk=4096), 4),
+])
+def test_noalloc_checks_match_workspace_entry_point(lib, kw, code):
+    """The allocation-free call reports argument errors exactly as fa_fwd_splitkv
+    does (the same checks in the same order), and Nq == 0 is a no-op that never
+    touches the device, so both hold without a GPU."""
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=128, Nk=128, d=64, scale=0.125, causal=0,
+             n_splits=4)
+    a.update(kw)
+    head = (a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"], a["d"], a["scale"],
+            a["causal"], a["n_splits"])
+    assert fa.fa_fwd_splitkv_noalloc(*head, None) == code
+    assert fa.fa_fwd_splitkv(*head, FAKE, 1 << 40, None) == code
+
+
+def test_noalloc_single_slice_needs_no_array(lib):
+    """One slice runs the plain kernel and uses no workspace, so a shape whose
+    slice buffers would not fit the fixed array is not refused for that: the
+    call gets past the size check (here to the device check, as no GPU is
+    present or the fake pointers are not device memory)."""
+    assert fa.fa_splitkv_workspace_bytes(1, 64, 4096, 4096, 128, 1) > fa.NOALLOC_SCRATCH_BYTES
+    st = fa.fa_fwd_splitkv_noalloc(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 64, 4096, 4096, 128, 0.125, 0, 1, None)
+    assert st in (6, 7, 10)  # FA_ERR_LAUNCH / FA_ERR_DEVICE / FA_ERR_POINTER, never FA_ERR_WORKSPACE
+
+
 def test_window_host_validation(lib):
     assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 64, 0.125, -2, 0, None) == 3
     assert fa.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 256, 64, 0.125, 0, -5, None) == 3
