@@ -9,6 +9,9 @@
 //   P = 2^(S*c - m_bar)           c = scale * log2(e) (section 4, exp2 form)
 //   l = alpha*l + rowsum P; O = alpha*O + P V_j   (GEMM-II into TMEM)
 // and at the end O / l and LSE = ln 2 * (m_bar + log2 l) (section 3, 5).
+// The l that divides O counts the row's largest P as rounded to bf16 for the
+// P V product (LSE keeps the exact l), so that a row dominated by one key
+// divides that key's rounded weight by itself.
 // The reference m_bar moves only when the candidate maximum exceeds it by
 // more than tau = 8 in base-2 units ("conditional softmax rescaling", page
 // "pinghaoyang FlashAttention 1-4 guide", FA4 section); the final division
@@ -440,6 +443,11 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
     const float NEG_INF = -__int_as_float(0x7f800000);
     float m_bar = NEG_INF;  // reference maximum, base-2 scaled units
     float l = 0.f;
+    // The row's largest score so far (raw units).  The reference only moves
+    // when a tile raises the row's maximum, so the reference in force when the
+    // largest score was exponentiated is the final m_bar: the epilogue can
+    // recompute that P bit for bit.
+    float r_max = NEG_INF;
     bool ok = true;
     const int nt = nkv[t];
     for (int j = 0; j < nt; ++j) {
@@ -499,7 +507,9 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
       }
 #pragma unroll
       for (int i = 2; i < 32; i += 2) mx2 = fmax3(mx2, f3[i], f3[i + 1]);
-      const float m_new = fmaxf(fmax3(mx0, mx1, mx2), mx3) * c;
+      const float s_max = fmaxf(fmax3(mx0, mx1, mx2), mx3);
+      r_max = fmaxf(r_max, s_max);
+      const float m_new = s_max * c;
       const bool need = m_new > m_bar + 8.0f;
       const bool any_need = __any_sync(0xffffffffu, need);
       float alpha = 1.0f;
@@ -556,7 +566,13 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
         report_wait_failure(abort_flag, 8u);
       } else {
         tc_fence_after();
-        const float inv_l = (l > 0.f) ? (1.0f / l) : 0.f;
+        // O's normaliser counts the row's largest P as rounded to bf16 for P V
+        float l_o = l;
+        if (l > 0.f) {
+          const float e_max = ex2(fmaf(r_max, c, -m_bar));
+          l_o += __uint_as_float(pack_bf16(e_max, 0.f) << 16) - e_max;
+        }
+        const float inv_l = (l > 0.f) ? (1.0f / l_o) : 0.f;
         const bool store = row < p.Nq;
         const size_t grow = static_cast<size_t>(bh) * p.Nq + row;  // row within [BH * Nq]
         if (!SPLIT) {

@@ -68,7 +68,9 @@ typedef enum {
  * Arithmetic: bf16 products accumulated in fp32 on the tensor cores, softmax
  * in fp32 (base-2 exponentials with log2(e) folded into the scale), the
  * probabilities rounded to bf16 for the P.V product, fp32 accumulation of O,
- * one division by the row sum at the end, O rounded to bf16 (nearest even).
+ * one division at the end by the row sum with the row's largest probability
+ * counted as rounded for P.V (so a row dominated by one key returns that
+ * key's V), O rounded to bf16 (nearest even).  LSE uses the exact fp32 sum.
  *
  * Ownership: the caller owns all five buffers; the library keeps no pointer
  * after the call returns and allocates nothing.

@@ -2,9 +2,17 @@
 through the C ABI binding, compare with the fp64 oracle.
 
 Tolerances (the stated bar, with the readings noted):
-  O:   |O_gpu - O_ref| <= 1e-2 * max(1, |O_ref|) elementwise.  Absolute 1e-2
-       at unit scale; relative above it, since a bf16 output holds only 8
-       significant bits (half an ulp exceeds 1e-2 once |O| >= 4).
+  O:   |O_gpu - O_ref| <= min(1e-2 * max(1, |O_ref|), 1e-2 + u(O_ref) / 2)
+       elementwise, u(x) the spacing of bf16 numbers at x (2^(floor(log2 |x|) - 7)).
+       O is returned in bf16, 8 significant bits, as the operation specifies;
+       rounding a value to bf16 moves it by up to u/2, between 2^-9 and 2^-8
+       of its magnitude, and the bf16 P of the P.V product moves the value
+       before that rounding by up to about 2^-8 of the spread of the V rows
+       it mixes.  The bar reads "max |dO| <= 1e-2" as an error of at most
+       1e-2 before the final rounding to bf16, plus that rounding: absolute
+       1e-2 below |O| = 1 (no looser than before anywhere), and 1e-2 + u/2
+       above (0.0178 on [2, 4), 0.0256 on [4, 8), against the 0.02-0.08 of a
+       relative 1e-2 * |O| there).
   LSE: |LSE_gpu - LSE_ref| <= 1e-3 * max(1, |LSE_ref|).
 """
 from __future__ import annotations
@@ -39,8 +47,20 @@ def run_gpu(q, k, v, scale, causal, n_splits=None):
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
 
+def o_tol(o_ref):
+    """Elementwise O bar: min(1e-2 * max(1, |O_ref|), 1e-2 + half the bf16 spacing at O_ref)."""
+    mag = np.abs(o_ref)
+    with np.errstate(divide="ignore"):
+        expo = np.floor(np.log2(np.where(mag > 0, mag, 1.0)))
+    half_ulp = np.where(mag > 0, np.exp2(expo - 8.0), 0.0)
+    return np.minimum(O_TOL * np.maximum(1.0, mag), O_TOL + half_ulp)
+
+
 def o_err(o_gpu, o_ref):
-    return float(np.max(np.abs(o_gpu - o_ref) / np.maximum(1.0, np.abs(o_ref)))) if o_ref.size else 0.0
+    """Largest |O_gpu - O_ref| / (o_tol(O_ref) / 1e-2): <= 1e-2 passes."""
+    if not o_ref.size:
+        return 0.0
+    return float(np.max(np.abs(o_gpu - o_ref) / (o_tol(o_ref) / O_TOL)))
 
 
 def lse_err(l_gpu, l_ref):

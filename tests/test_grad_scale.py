@@ -1,10 +1,33 @@
-"""CPU checks of the backward parity bar's row scales (grad_scale), which are
-not expected values; the expected values come from the backward oracle."""
+"""CPU checks of the parity bars' helpers: the forward O bar (parity_util.o_tol)
+and the backward row scales (grad_scale), neither of which is an expected
+value; the expected values come from the oracles."""
 import numpy as np
 import pytest
 
 import synth
 from grad_scale import dkdv_key_scales, dq_row_scales, keep_matrix, row_scales
+from parity_util import o_tol
+
+
+def test_o_tol_values():
+    # absolute 1e-2 below |O| = 1; 1e-2 + half the bf16 spacing above it (capped by 1e-2 * |O|)
+    x = np.array([0.0, 0.5, -0.99, 1.0, 1.5, 3.0, -3.0, 6.0, 100.0])
+    want = np.array([1e-2, 1e-2, 1e-2, 1e-2, min(1.5e-2, 1e-2 + 2 ** -8), 1e-2 + 2 ** -7, 1e-2 + 2 ** -7,
+                     1e-2 + 2 ** -6, 1e-2 + 2 ** -2])
+    assert np.allclose(o_tol(x), want, rtol=0, atol=1e-15)
+
+
+def test_o_tol_half_spacing_is_the_bf16_spacing():
+    """u/2 in the bar is half the distance from a bf16 number to its upper neighbour."""
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(2000) * np.exp2(rng.integers(-6, 8, 2000))).astype(np.float32)
+    bits = synth.f32_to_bf16_bits(x)
+    xb = synth.bf16_to_f32(bits).astype(np.float64)
+    up = synth.bf16_to_f32((bits & 0x8000) | ((bits & 0x7FFF) + 1)).astype(np.float64)
+    half_spacing = np.abs(up - xb) / 2
+    # o_tol - 1e-2 is u/2 wherever the 1e-2 * |O| cap does not bind (|O| >= 1.4)
+    sel = np.abs(xb) >= 1.4
+    assert np.allclose(o_tol(xb[sel]) - 1e-2, half_spacing[sel], rtol=1e-12, atol=0)
 
 
 def _case(seed, nq=70, nk=90, d=16, window=None, causal=False):
