@@ -22,7 +22,9 @@
 //   warps 4-7  the same for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through
 //              one ring of kRing tile-sized slots (mbarrier full/empty per slot)
-//   warp  9    MMA issuer: tcgen05.mma (one thread), commits to mbarriers
+//   warp  9    MMA issuer: tcgen05.mma and commits to mbarriers, issued by one
+//              thread (d = 128: lane 0 runs the loop alone; d = 64: the whole
+//              warp runs it and one elected lane issues)
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D);
 //   P_i (bf16, packed in pairs) overwrites the first 64 columns of S_i and is
@@ -279,7 +281,29 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
     }
   } else if (warp == C::kWarpMma) {
     // ======================= MMA issuer ====================================
-    if (lane == 0) {
+    // d = 64: the whole warp runs the issue loop on warp-uniform values and
+    // one elected lane issues each tcgen05.mma and commit (same-box A/B:
+    // +4% on 4 x 32 x 8192, +6% on 8 x 12 x 1024 causal); d = 128: lane 0
+    // alone runs it (the elected form measured 1-1.6% slower there).
+    constexpr bool kElect = (D == 64);
+    auto mma_ss_x = [](uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+      if constexpr (kElect) mma_ss_elect(d_tmem, a_desc, b_desc, idesc, acc);
+      else mma_ss(d_tmem, a_desc, b_desc, idesc, acc);
+    };
+    auto mma_ts_x = [](uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+      if constexpr (kElect) mma_ts_elect(d_tmem, a_tmem, b_desc, idesc, acc);
+      else mma_ts(d_tmem, a_tmem, b_desc, idesc, acc);
+    };
+    auto commit_x = [](uint32_t b) {
+      if constexpr (kElect) mma_commit_elect(b);
+      else mma_commit(b);
+    };
+    // a wait's outcome, the same for every lane that runs the loop
+    auto uniform = [](bool v) -> bool {
+      if constexpr (kElect) return __all_sync(0xffffffffu, v);
+      else return v;
+    };
+    if (kElect || lane == 0) {
       // descriptors: start address lives in bits 0-13 (address >> 4), so a
       // byte offset is added to a base descriptor as (offset >> 4)
       const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
@@ -294,32 +318,33 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss(tS[t], dq + off, dk + off, C::kIdescS, kk > 0 ? 1u : 0u);
+          mma_ss_x(tS[t], dq + off, dk + off, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       auto gemm2 = [&](int t, int slot, bool acc_prev) {
         const uint64_t dv = dV0 + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < C::kBN / 16; ++kk)
-          mma_ts(tO[t], tS[t] + kk * 8, dv + ((kk * 2048) >> 4), C::kIdescO, (acc_prev || kk > 0) ? 1u : 0u);
+          mma_ts_x(tO[t], tS[t] + kk * 8, dv + ((kk * 2048) >> 4), C::kIdescO, (acc_prev || kk > 0) ? 1u : 0u);
       };
       auto wait_item = [&](int item) -> bool {
-        return mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, abort_flag);
+        return uniform(mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, abort_flag));
       };
+      auto uwait = [&](uint32_t b, uint32_t ph) -> bool { return uniform(mbar_wait(b, ph, abort_flag)); };
       // is K/V tile j (absolute index within the head) visible to query tile t?
       auto in_range = [&](int t, int j) -> bool { return j >= jlo[t] && j < jhi[t]; };
       bool ok = true;
       for (int t = 0; t < 2 && ok; ++t)
-        if (nkv[t] > 0) ok = mbar_wait(bar(kBarQ + t), 0, abort_flag);
+        if (nkv[t] > 0) ok = uwait(bar(kBarQ + t), 0);
       if (ok && n_max > 0) ok = wait_item(0);
       if (ok && n_max > 0) {
         tc_fence_after();
         for (int t = 0; t < 2; ++t)
           if (nkv[t] > 0 && jlo[t] == J0) {
             gemm1(t, 0);
-            mma_commit(bar(kBarS + t));
+            commit_x(bar(kBarS + t));
           }
-        mma_commit(empty(0));
+        commit_x(empty(0));
       }
       // Issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), with
       // every barrier check of the first half gathered in one place (each
@@ -336,33 +361,33 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
           const bool a = mbar_try_wait(full(sv), (iv / C::kRing) & 1);
           const bool b = !has_next || mbar_try_wait(full(sk), (ik / C::kRing) & 1);
           const bool c = !pv0 || mbar_try_wait(bar(kBarP + 0), (j - jlo[0]) & 1);
-          if (!(a && b && c)) {
+          if (!uniform(a && b && c)) {
             if (!wait_item(iv)) return false;
             if (has_next && !wait_item(ik)) return false;
-            if (pv0 && !mbar_wait(bar(kBarP + 0), (j - jlo[0]) & 1, abort_flag)) return false;
+            if (pv0 && !uwait(bar(kBarP + 0), (j - jlo[0]) & 1)) return false;
           }
         }
         tc_fence_after();
         if (pv0) {
           gemm2(0, sv, j > jlo[0]);
-          if (j == jhi[0] - 1) mma_commit(bar(kBarO + 0));
+          if (j == jhi[0] - 1) commit_x(bar(kBarO + 0));
         }
         if (has_next && in_range(0, j + 1)) {
           gemm1(0, sk);
-          mma_commit(bar(kBarS + 0));
+          commit_x(bar(kBarS + 0));
         }
         if (pv1) {
-          if (!mbar_wait(bar(kBarP + 1), (j - jlo[1]) & 1, abort_flag)) return false;
+          if (!uwait(bar(kBarP + 1), (j - jlo[1]) & 1)) return false;
           tc_fence_after();
           gemm2(1, sv, j > jlo[1]);
-          if (j == jhi[1] - 1) mma_commit(bar(kBarO + 1));
+          if (j == jhi[1] - 1) commit_x(bar(kBarO + 1));
         }
-        mma_commit(empty(sv));
+        commit_x(empty(sv));
         if (has_next && in_range(1, j + 1)) {
           gemm1(1, sk);
-          mma_commit(bar(kBarS + 1));
+          commit_x(bar(kBarS + 1));
         }
-        if (has_next) mma_commit(empty(sk));
+        if (has_next) commit_x(empty(sk));
         return true;
       };
       // The steady state: K/V tiles j with j - 1, j and j + 1 in both query
@@ -379,24 +404,22 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
         const bool a = mbar_try_wait(full(sv), phv);
         const bool b = mbar_try_wait(full(sk), phk);
         const bool c = mbar_try_wait(bar(kBarP + 0), ph0);
-        if (!(a && b && c)) {
-          if (!mbar_wait(full(sv), phv, abort_flag) || !mbar_wait(full(sk), phk, abort_flag) ||
-              !mbar_wait(bar(kBarP + 0), ph0, abort_flag))
-            return false;
+        if (!uniform(a && b && c)) {
+          if (!uwait(full(sv), phv) || !uwait(full(sk), phk) || !uwait(bar(kBarP + 0), ph0)) return false;
         }
         tc_fence_after();
         gemm2(0, sv, true);
         gemm1(0, sk);
-        mma_commit(bar(kBarS + 0));
-        if (!mbar_try_wait(bar(kBarP + 1), ph1)) {
-          if (!mbar_wait(bar(kBarP + 1), ph1, abort_flag)) return false;
+        commit_x(bar(kBarS + 0));
+        if (!uniform(mbar_try_wait(bar(kBarP + 1), ph1))) {
+          if (!uwait(bar(kBarP + 1), ph1)) return false;
         }
         tc_fence_after();
         gemm2(1, sv, true);
-        mma_commit(empty(sv));
+        commit_x(empty(sv));
         gemm1(1, sk);
-        mma_commit(bar(kBarS + 1));
-        mma_commit(empty(sk));
+        commit_x(bar(kBarS + 1));
+        commit_x(empty(sk));
         return true;
       };
       // steady range [s_lo, s_hi) of jj; the tiles before and after it take
@@ -416,7 +439,7 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
       for (; ok && jj < n_max; ++jj) ok = general(jj);
       if (!ok) report_wait_failure(abort_flag, 4u);
       // Drain: every MMA issued so far has completed once this barrier flips.
-      mma_commit(bar(kBarDrain));
+      commit_x(bar(kBarDrain));
       mbar_wait(bar(kBarDrain), 0, nullptr);
     }
   } else {
