@@ -22,9 +22,8 @@
 //   warps 4-7  the same for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through
 //              one ring of kRing tile-sized slots (mbarrier full/empty per slot)
-//   warp  9    MMA issuer: tcgen05.mma and commits to mbarriers, issued by one
-//              thread (d = 128: lane 0 runs the loop alone; d = 64: the whole
-//              warp runs it and one elected lane issues)
+//   warp  9    MMA issuer: the whole warp runs the loop, one elected lane
+//              issues every tcgen05.mma and commit to mbarriers
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D);
 //   P_i (bf16, packed in pairs) overwrites the first 64 columns of S_i and is
@@ -281,29 +280,20 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
     }
   } else if (warp == C::kWarpMma) {
     // ======================= MMA issuer ====================================
-    // d = 64: the whole warp runs the issue loop on warp-uniform values and
-    // one elected lane issues each tcgen05.mma and commit (same-box A/B:
-    // +4% on 4 x 32 x 8192, +6% on 8 x 12 x 1024 causal); d = 128: lane 0
-    // alone runs it (the elected form measured 1-1.6% slower there).
-    constexpr bool kElect = (D == 64);
+    // The whole warp runs the issue loop on warp-uniform values (every
+    // barrier outcome made uniform with a vote); one lane chosen by
+    // elect.sync issues each tcgen05.mma and commit, with no branch around the
+    // instruction.  Same-box A/B against lane 0 alone: +4% to +7.5% at d = 64,
+    // and at d = 128 +1% together with the branch-free steady body below.
     auto mma_ss_x = [](uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
-      if constexpr (kElect) mma_ss_elect(d_tmem, a_desc, b_desc, idesc, acc);
-      else mma_ss(d_tmem, a_desc, b_desc, idesc, acc);
+      mma_ss_elect(d_tmem, a_desc, b_desc, idesc, acc);
     };
     auto mma_ts_x = [](uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
-      if constexpr (kElect) mma_ts_elect(d_tmem, a_tmem, b_desc, idesc, acc);
-      else mma_ts(d_tmem, a_tmem, b_desc, idesc, acc);
+      mma_ts_elect(d_tmem, a_tmem, b_desc, idesc, acc);
     };
-    auto commit_x = [](uint32_t b) {
-      if constexpr (kElect) mma_commit_elect(b);
-      else mma_commit(b);
-    };
-    // a wait's outcome, the same for every lane that runs the loop
-    auto uniform = [](bool v) -> bool {
-      if constexpr (kElect) return __all_sync(0xffffffffu, v);
-      else return v;
-    };
-    if (kElect || lane == 0) {
+    auto commit_x = [](uint32_t b) { mma_commit_elect(b); };
+    auto uniform = [](bool v) -> bool { return __all_sync(0xffffffffu, v); };
+    {
       // descriptors: start address lives in bits 0-13 (address >> 4), so a
       // byte offset is added to a base descriptor as (offset >> 4)
       const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
@@ -423,10 +413,10 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
         return true;
       };
       // steady range [s_lo, s_hi) of jj; the tiles before and after it take
-      // the general body.  Used at d = 64 only: there it gains 4%, at d = 128
-      // (MMA groups twice as long per check) it measured 3% slower.
+      // the general body.  With the elected issue it gains at both head sizes
+      // (with lane 0 alone it had measured 3% slower at d = 128).
       int s_lo = n_max, s_hi = n_max;
-      if (D == 64 && nkv[0] > 0 && nkv[1] > 0) {
+      if (nkv[0] > 0 && nkv[1] > 0) {
         const int lo = max(jlo[0], jlo[1]) + 1 - J0, hi = min(jhi[0], jhi[1]) - 1 - J0;
         if (lo < hi) {
           s_lo = lo;
