@@ -38,9 +38,8 @@ METRIC = "attention fwd TFLOP/s and % of GB300 dense BF16 peak (1 GPU)"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "long_8192_d128"
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_NAME = "fa_fwd_kernel"
-KERNEL_SOURCES = ["exact_attention_19_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_19_gb300/csrc/fa_ptx.cuh",
-                  "exact_attention_19_gb300/csrc/fa_api.cu"]
+KERNEL_SOURCES = ["exact_attention_19_gb300/csrc/fa_fwd_kernel.cuh", "exact_attention_19_gb300/csrc/fa_fwd_persist.cuh",
+                  "exact_attention_19_gb300/csrc/fa_ptx.cuh", "exact_attention_19_gb300/csrc/fa_api.cu"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "fa_fwd_kernel_dram_traffic.md")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 NOMINAL_BF16_TFLOPS = 2250.0  # nominal dense bf16 tensor peak of one GB300 (not measured; context only)
@@ -55,6 +54,15 @@ def kernel_source_hash() -> str:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def kernel_name(w, n_splits) -> str:
+    """The forward kernel the library launches for this workload: the persistent one for a single
+    pass at d = 128 without a mask (fa_fwd and fa_fwd_splitkv with one split), else fa_fwd_kernel."""
+    single = n_splits is None or n_splits <= 1
+    if single and w.d == 128 and not w.causal and w.window is None:
+        return "fa_fwd_persist_kernel"
+    return "fa_fwd_kernel"
 
 
 def read_traffic(workload: str, src_hash: str):
@@ -515,7 +523,7 @@ def run_gpu(args, w: synth.Workload, rank: int, world: int, local_rank: int):
     roofline.update({"traffic": traffic, "peak_kind": f"{roofline['peak_kind']}, {peaks_kind}",
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                      "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
-                     "kernel": KERNEL_NAME, "kernel_source": src_hash,
+                     "kernel": kernel_name(w, n_splits), "kernel_source": src_hash,
                      "algorithmic_bytes": w.algorithmic_bytes})
 
     # third roofline: exponentials (one ex2 per visible score) per SM clock

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libfa_gb300.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("fa_api.cu", "fa_probe.cu", "fa_selftest.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_ptx.cuh", "fa_fwd_kernel.cuh", "fa_bwd_kernel.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("fa_ptx.cuh", "fa_fwd_kernel.cuh", "fa_fwd_persist.cuh", "fa_bwd_kernel.cuh")] + [
     os.path.join(INCLUDE, "fa.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

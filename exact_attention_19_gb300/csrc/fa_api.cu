@@ -11,6 +11,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_fwd_persist.cuh"
 #include "fa_bwd_kernel.cuh"
 
 namespace {
@@ -76,6 +77,9 @@ bool set_smem_attrs() {
             set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
+  if constexpr (D == 128)
+    ok = ok && cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(fa::PCfg<128>::kSmemBytes)) == cudaSuccess;
   if constexpr (D == 64)
     ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess &&
          set_smem_attr<64, fa::kMaskNone, true, 1>() == cudaSuccess &&
@@ -259,10 +263,29 @@ void split_shape(int Nk, int n_splits, int* split_tiles, int* eff_splits) {
   *eff_splits = (n_kv + *split_tiles - 1) / *split_tiles;
 }
 
+// The persistent d = 128 kernel: one CTA per multiprocessor, at most one per
+// work unit (a head's pair of 128-row query tiles).
+int launch_persist128(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
+                      long long n_units, int sms, cudaStream_t stream) {
+  using C = fa::PCfg<128>;
+  if (n_units >= (1ll << 31)) return FA_ERR_SHAPE;
+  const long long grid = n_units < sms ? n_units : sms;
+  fa::fa_fwd_persist_kernel<128><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
+      mq, mk, mv, p, static_cast<int>(n_units));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
 // Single-pass forward (no mask or causal) on prepared maps and parameters.
+// d = 128 without a mask: the persistent kernel (units of equal length,
+// balanced by its static schedule).  Causal: one CTA per unit, so the
+// hardware's dispatch balances units of unequal length in their longest-first
+// launch order; d = 64: one CTA per unit as well (measured as fast).
 int launch_single_pass(int B, int H, int Nq, int Nk, int d, int causal, const CUtensorMap& mq,
                        const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, fa::FwdParams p,
-                       cudaStream_t stream) {
+                       int dev, cudaStream_t stream) {
+  if (d == 128 && !causal)
+    return launch_persist128(mq, mk, mv, p, static_cast<long long>(B) * H * p.n_pairs, g_dev_sms_or(dev, 148),
+                             stream);
   if (d == 64 && causal && Nk <= kSingleTileMaxKeys) {
     p.n_pairs = (Nq + 127) / 128;  // one query tile per CTA
     const long long grid = static_cast<long long>(B) * H * p.n_pairs;
@@ -306,7 +329,7 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   bool noop = false;
   const int st = prepare_call(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &mo, &p, &dev, &noop);
   if (st != FA_OK || noop) return st;
-  return launch_single_pass(B, H, Nq, Nk, d, causal, mq, mk, mv, mo, p, stream);
+  return launch_single_pass(B, H, Nq, Nk, d, causal, mq, mk, mv, mo, p, dev, stream);
 }
 
 int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
@@ -410,7 +433,7 @@ int splitkv_impl(const void* q, const void* k, const void* v, void* o, float* ls
   int dev = -1;
   st = prepare_launch(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, &mq, &mk, &mv, &mo, &p, &dev);
   if (st != FA_OK) return st;
-  if (eff == 1) return launch_single_pass(B, H, Nq, Nk, d, causal, mq, mk, mv, mo, p, stream);
+  if (eff == 1) return launch_single_pass(B, H, Nq, Nk, d, causal, mq, mk, mv, mo, p, dev, stream);
   if (noalloc) {
     // Every partial the merge reads is written earlier in the same call (an
     // empty slice writes weight 2^-inf), so nothing in the array is cleared.

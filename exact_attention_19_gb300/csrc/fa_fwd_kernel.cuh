@@ -243,7 +243,24 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
 
   if (warp == C::kWarpProd) {
     // ======================= TMA producer =================================
-    if (lane == 0) {
+    // d = 64: the whole warp runs the loop (each barrier outcome made uniform
+    // with a vote) and one lane chosen by elect.sync issues every expect-tx
+    // and copy, as in the MMA issuer below.  A d = 64 K/V tile carries half
+    // the MMA work of a d = 128 one, so the producer's issue latency weighs
+    // twice as much there.  d = 128: lane 0 alone.
+    auto uniform = [](bool v) -> bool {
+      if constexpr (D == 64) return __all_sync(0xffffffffu, v);
+      else return v;
+    };
+    auto expect_tx = [](uint32_t b, uint32_t bytes) {
+      if constexpr (D == 64) mbar_arrive_expect_tx_elect(b, bytes);
+      else mbar_arrive_expect_tx(b, bytes);
+    };
+    auto load = [](uint32_t dst, const CUtensorMap* map, uint32_t b, int x, int y, int z) {
+      if constexpr (D == 64) tma_load_3d_elect(dst, map, b, x, y, z);
+      else tma_load_3d(dst, map, b, x, y, z);
+    };
+    if (D == 64 || lane == 0) {
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
@@ -251,31 +268,31 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
       for (int t = 0; t < 2; ++t) {
         if (nkv[t] == 0) continue;
         const uint32_t dst = base + C::kQOff + t * C::kTileBytes;
-        mbar_arrive_expect_tx(bar(kBarQ + t), C::kTileBytes);
+        expect_tx(bar(kBarQ + t), C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(dst + b * C::kBoxBytes, &tmQ, bar(kBarQ + t), b * 64, row0[t], bh);
+          load(dst + b * C::kBoxBytes, &tmQ, bar(kBarQ + t), b * 64, row0[t], bh);
       }
       int issued = 0;
       for (int item = 0; item < n_items; ++item) {
         const int s = item % C::kRing;
         const uint32_t ph = (item / C::kRing) & 1;
-        if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
+        if (!uniform(mbar_wait(empty(s), ph ^ 1u, abort_flag))) {
           report_wait_failure(abort_flag, 2u);
           break;
         }
         const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
-        mbar_arrive_expect_tx(full(s), C::kTileBytes);
+        expect_tx(full(s), C::kTileBytes);
         for (int b = 0; b < C::kBoxes; ++b)
-          tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (J0 + (item >> 1)) * C::kBN, bh);
+          load(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (J0 + (item >> 1)) * C::kBN, bh);
         issued = item + 1;
       }
       if (*abort_flag) {
         // Let every copy already issued land before the CTA can exit: the
         // last item issued into each slot is among the final kRing items.
         for (int item = max(0, issued - C::kRing); item < issued; ++item)
-          mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, nullptr);
+          uniform(mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, nullptr));
         for (int t = 0; t < 2; ++t)
-          if (nkv[t] > 0) mbar_wait(bar(kBarQ + t), 0, nullptr);
+          if (nkv[t] > 0) uniform(mbar_wait(bar(kBarQ + t), 0, nullptr));
       }
     }
   } else if (warp == C::kWarpMma) {

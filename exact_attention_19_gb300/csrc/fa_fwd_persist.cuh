@@ -1,0 +1,620 @@
+// fa_fwd_persist.cuh -- persistent fused exact-attention forward for sm_103a
+// (d = 128, no mask, no K/V split).
+//
+// The arithmetic is that of fa_fwd_kernel (FA2 loop order, page "llm-infra-
+// atlas / FlashAttention 01", sections 2-4; conditional rescaling with
+// tau = 8 in base 2, page "pinghaoyang FlashAttention 1-4 guide", FA4
+// section; O divided by the row sum with the row's largest P counted as
+// rounded to bf16).  What differs is the schedule:
+//
+//  * One CTA per SM loops over work units (b*H + h, pair of 128-row query
+//    tiles); CTA c takes units c, 2G-1-c, 2G+c, ... (G CTAs).  The K/V ring,
+//    the S and P barriers and the MMA stream run on across unit boundaries:
+//    in the last K/V step of a unit the MMA issuer computes the next unit's
+//    first S products where it would otherwise compute the next tile's, so
+//    the tensor pipe sees no start or end of a unit, and no CTA is launched,
+//    set up or torn down per unit.
+//  * 12 warps, every one with the same 168 registers:
+//      warps 0-3   softmax, conditional rescale and epilogue of query tile 0
+//      warps 4-7   the same for query tile 1
+//      warp  8     TMA producer of the K/V ring
+//      warp  9     MMA issuer: the whole warp runs the issue loop on
+//                  warp-uniform values, one elected lane issues
+//                  (as in fa_fwd_kernel)
+//      warp 10     TMA producer of the Q tiles (and an L2 prefetch of the
+//                  next unit's Q)
+//      warp 11     idle
+//    The epilogue of a unit's tile (O / l to bf16, stored by each row's
+//    thread; LSE) runs in that tile's softmax warps before they take the next
+//    unit's first S, so the next unit's first P V (which overwrites O) cannot
+//    start before O has been read.
+//  * One Q buffer per tile; the next unit's Q is loaded as soon as the last S
+//    product of the unit has read the old one (it was prefetched into L2 a
+//    unit earlier).  The Q-buffer bookkeeping below is written for kQBufs
+//    buffers per tile; at d = 128 shared memory holds one.
+//  * Only d = 128 without a mask is built: at d = 64 this schedule measured
+//    no faster than fa_fwd_kernel's one-CTA-per-unit launch, and causal units
+//    of unequal length are balanced better by the hardware's dispatch of
+//    fa_fwd_kernel's longest-first grid than by a static schedule.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+template <int D>
+struct PCfg {
+  static_assert(D == 128, "the persistent schedule is built for d = 128 only");
+  static constexpr int kThreads = 384;  // three warpgroups: the registers of 10 warps' worth are allocated anyway
+  static constexpr int kWarpKV = 8, kWarpMma = 9, kWarpQ = 10;
+  static constexpr int kBM = 128, kBN = 128;
+  static constexpr int kQBufs = 1;  // Q buffers per query tile
+  static constexpr int kRing = 5;   // K/V ring slots
+  static constexpr int kBoxes = D / 64;
+  static constexpr uint32_t kBoxBytes = 128u * 128u;
+  static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
+  static constexpr uint32_t kQOff = 0;  // Q[qb][t] at (2 * qb + t) * kTileBytes
+  static constexpr uint32_t kRingOff = 2 * kQBufs * kTileBytes;
+  static constexpr uint32_t kBarOff = kRingOff + kRing * kTileBytes;
+  static constexpr uint32_t kBarBytes = 512;
+  static constexpr uint32_t kSmemBytes = kBarOff + kBarBytes + 1024;  // + alignment slack
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmO = 256;  // O[t] at kTmO + t * D
+  static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
+  static constexpr uint32_t kIdescO = idesc_bf16(128, D, true);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// barrier slots (8 bytes each)
+enum : int {
+  kPBarQFull = 0,    // [qb][t]: 4
+  kPBarQFree = 4,    // [qb][t]: 4
+  kPBarS = 8,        // [t]
+  kPBarP = 10,       // [t]
+  kPBarOFinal = 12,  // [t]
+  kPBarDrain = 14,
+  kPBarRing = 15     // full[kRing] then empty[kRing]
+};
+static_assert(8 * (kPBarRing + 16) <= 448, "barrier block");
+
+// L2 prefetch of one TMA box (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// One work unit as every role sees it.
+struct PUnit {
+  int bh;
+  int row0[2];
+  int jhi[2];      // K/V tiles [0, jhi[t]) visible to query tile t (0 when the tile is absent)
+  int n_max;       // K/V tiles streamed: max(jhi)
+};
+
+template <int D>
+__global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
+    fa_fwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV, const FwdParams p, const int n_units) {
+  using C = PCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_addr(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* const sbase = smem_raw + (base - raw_addr);
+
+  const uint32_t bar0 = base + C::kBarOff;
+  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+  auto full = [&](int slot) -> uint32_t { return bar(kPBarRing + slot); };
+  auto empty = [&](int slot) -> uint32_t { return bar(kPBarRing + C::kRing + slot); };
+  auto slot_addr = [&](int slot) -> uint32_t { return base + C::kRingOff + slot * C::kTileBytes; };
+  auto q_addr = [&](int qb, int t) -> uint32_t { return base + C::kQOff + (2 * qb + t) * C::kTileBytes; };
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + C::kBarOff + kTmemSlotOff);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + C::kBarOff + kAbortOff);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(kPBarQFull + i), 1);
+      mbar_init(bar(kPBarQFree + i), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kPBarS + t), 1);
+      mbar_init(bar(kPBarP + t), 128);
+      mbar_init(bar(kPBarOFinal + t), 1);
+    }
+    mbar_init(bar(kPBarDrain), 1);
+    for (int s = 0; s < C::kRing; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == C::kWarpMma) {
+    tmem_alloc(smem_addr(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // ---- the CTA's work units ---------------------------------------------
+  const int G = static_cast<int>(gridDim.x);
+  const int cta = static_cast<int>(blockIdx.x);
+  const int n_kv = (p.Nk + C::kBN - 1) / C::kBN;
+  // k-th unit of this CTA, or false past the end
+  auto unit_at = [&](int k, PUnit& u) -> bool {
+    const long long id = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - cta) : cta);
+    if (id >= n_units) return false;
+    const int uid = static_cast<int>(id);
+    const int pair = uid % p.n_pairs;
+    u.bh = uid / p.n_pairs;
+    u.n_max = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const int qt = 2 * pair + t;
+      u.row0[t] = qt * C::kBM;
+      u.jhi[t] = 0;
+      if (u.row0[t] < p.Nq) u.jhi[t] = n_kv;
+      u.n_max = max(u.n_max, u.jhi[t]);
+    }
+    return true;
+  };
+
+  if (warp >= 8) {
+    if (warp == C::kWarpKV && lane == 0) {
+      // ======================= K/V producer ===============================
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      int issued = 0;
+      bool ok = true;
+      PUnit u;
+      for (int k = 0; ok && unit_at(k, u); ++k) {
+        for (int i = 0; i < 2 * u.n_max; ++i) {
+          const int item = issued;
+          const int s = item % C::kRing;
+          if (!mbar_wait(empty(s), ((item / C::kRing) & 1) ^ 1u, abort_flag)) {
+            report_wait_failure(abort_flag, 2u);
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
+          mbar_arrive_expect_tx(full(s), C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (i >> 1) * C::kBN, u.bh);
+          issued = item + 1;
+        }
+      }
+      if (*abort_flag) {
+        // let every copy already issued land before the CTA can exit
+        for (int item = max(0, issued - C::kRing); item < issued; ++item)
+          mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, nullptr);
+      }
+    } else if (warp == C::kWarpQ && lane == 0) {
+      // ======================= Q producer =================================
+      tma_prefetch_map(&tmQ);
+      int occ[2] = {0, 0};
+      bool ok = true;
+      PUnit u, un;
+      for (int k = 0; ok && unit_at(k, u); ++k) {
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (u.jhi[t] == 0) continue;
+          const int qb = occ[t] % C::kQBufs, use = occ[t] / C::kQBufs;
+          if (use > 0 && !mbar_wait(bar(kPBarQFree + 2 * qb + t), (use - 1) & 1, abort_flag)) {
+            report_wait_failure(abort_flag, 2u);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kPBarQFull + 2 * qb + t), C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            tma_load_3d(q_addr(qb, t) + b * C::kBoxBytes, &tmQ, bar(kPBarQFull + 2 * qb + t), b * 64, u.row0[t],
+                        u.bh);
+          ++occ[t];
+        }
+        // the next unit's Q into L2 while this one runs
+        if (ok && unit_at(k + 1, un)) {
+          for (int t = 0; t < 2; ++t)
+            if (un.jhi[t] > 0)
+              for (int b = 0; b < C::kBoxes; ++b) tma_prefetch_l2_3d(&tmQ, b * 64, un.row0[t], un.bh);
+        }
+      }
+      if (*abort_flag) {
+        // every Q copy issued lands before exit: the last fill of each buffer
+        for (int t = 0; t < 2; ++t)
+          for (int i = max(0, occ[t] - C::kQBufs); i < occ[t]; ++i)
+            mbar_wait(bar(kPBarQFull + 2 * (i % C::kQBufs) + t), (i / C::kQBufs) & 1, nullptr);
+      }
+    } else if (warp == C::kWarpMma) {
+      // ======================= MMA issuer ==================================
+      // Every lane runs this loop; waits are made warp-uniform with
+      // __all_sync, and each tcgen05.mma / commit is issued by the lane that
+      // elect.sync picks inside the same asm statement.
+      auto uniform = [](bool v) -> bool { return __all_sync(0xffffffffu, v); };
+      // Per K/V step j of a unit, as in fa_fwd_kernel:
+      //   [V_j, K_{j+1}, P_0(j)] PV_0(j), S_0(j+1); [P_1(j)] PV_1(j), S_1(j+1)
+      // The interior steps of a unit run the same bodies as fa_fwd_kernel
+      // (the general one, and the branch-free copy where both tiles are
+      // inside their ranges); the last step computes the next unit's first
+      // S products (after checking its Q tiles) in place of S(j+1).  O needs no
+      // check: a tile's next first P V waits for its P, which that tile's
+      // softmax warps hand over only after their epilogue has read O.
+      const uint64_t dK0 = sdesc_sw128(base + C::kRingOff, 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(base + C::kRingOff, C::kBoxBytes, 1024);
+      const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
+      const uint32_t tS[2] = {tmem, tmem + 128u};
+      uint64_t dq[2] = {dQ0, dQ0}, dq_n[2] = {dQ0, dQ0};  // Q descriptors of the unit's and the next unit's tiles
+      const uint32_t to[2] = {tmem + C::kTmO, tmem + C::kTmO + D};
+      int qb[2] = {0, 0}, qb_n[2] = {0, 0};
+      auto gemm1 = [&](int t, uint64_t dqt, int slot) {
+        const uint64_t dk = dK0 + ((slot * C::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+          mma_ss_elect(tS[t], dqt + off, dk + off, C::kIdescS, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto gemm2 = [&](int t, int slot, bool acc_prev) {
+        const uint64_t dv = dV0 + ((slot * C::kTileBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < C::kBN / 16; ++kk)
+          mma_ts_elect(to[t], tS[t] + kk * 8, dv + ((kk * 2048) >> 4), C::kIdescO, (acc_prev || kk > 0) ? 1u : 0u);
+      };
+      auto qdesc = [&](int b, int t) -> uint64_t { return dQ0 + (((2 * b + t) * C::kTileBytes) >> 4); };
+      int np[2] = {0, 0};  // P phases consumed per tile
+      bool ok = true;
+      PUnit cur = {}, nxt = {};
+      bool has_nxt = false;
+      int base_item = 0;
+      int occ[2] = {0, 0}, occ_n[2] = {0, 0};
+      // interior step (1 <= jj <= n_max - 2): the general body
+      auto inner = [&](int jj) -> bool {
+        const int iv = base_item + 2 * jj + 1, ik = iv + 1;
+        const int sv = iv % C::kRing, sk = ik % C::kRing;
+        const bool pv0 = jj < cur.jhi[0], pv1 = jj < cur.jhi[1];
+        {
+          const bool a = mbar_try_wait(full(sv), (iv / C::kRing) & 1);
+          const bool b = mbar_try_wait(full(sk), (ik / C::kRing) & 1);
+          const bool c = !pv0 || mbar_try_wait(bar(kPBarP + 0), np[0] & 1);
+          if (!uniform(a && b && c)) {
+            if (!uniform(mbar_wait(full(sv), (iv / C::kRing) & 1, abort_flag))) return false;
+            if (!uniform(mbar_wait(full(sk), (ik / C::kRing) & 1, abort_flag))) return false;
+            if (pv0 && !uniform(mbar_wait(bar(kPBarP + 0), np[0] & 1, abort_flag))) return false;
+          }
+        }
+        tc_fence_after();
+        if (pv0) {
+          ++np[0];
+          gemm2(0, sv, true);
+          if (jj == cur.jhi[0] - 1) mma_commit_elect(bar(kPBarOFinal + 0));
+        }
+        if (jj + 1 < cur.jhi[0]) {
+          gemm1(0, dq[0], sk);
+          mma_commit_elect(bar(kPBarS + 0));
+          if (jj + 2 == cur.jhi[0]) mma_commit_elect(bar(kPBarQFree + 2 * qb[0] + 0));
+        }
+        if (pv1) {
+          if (!uniform(mbar_wait(bar(kPBarP + 1), np[1] & 1, abort_flag))) return false;
+          ++np[1];
+          tc_fence_after();
+          gemm2(1, sv, true);
+          if (jj == cur.jhi[1] - 1) mma_commit_elect(bar(kPBarOFinal + 1));
+        }
+        mma_commit_elect(empty(sv));
+        if (jj + 1 < cur.jhi[1]) {
+          gemm1(1, dq[1], sk);
+          mma_commit_elect(bar(kPBarS + 1));
+          if (jj + 2 == cur.jhi[1]) mma_commit_elect(bar(kPBarQFree + 2 * qb[1] + 1));
+        }
+        mma_commit_elect(empty(sk));
+        return true;
+      };
+      // interior step with both tiles inside their ranges and no tile's last
+      // S or P V in it: every product issued, no branch around the MMAs
+      auto steady = [&](int jj) -> bool {
+        const int iv = base_item + 2 * jj + 1, ik = iv + 1;
+        const int sv = iv % C::kRing, sk = ik % C::kRing;
+        const uint32_t phv = (iv / C::kRing) & 1, phk = (ik / C::kRing) & 1;
+        const uint32_t ph0 = np[0] & 1, ph1 = np[1] & 1;
+        const bool a = mbar_try_wait(full(sv), phv);
+        const bool b = mbar_try_wait(full(sk), phk);
+        const bool c = mbar_try_wait(bar(kPBarP + 0), ph0);
+        if (!uniform(a && b && c)) {
+          if (!uniform(mbar_wait(full(sv), phv, abort_flag)) || !uniform(mbar_wait(full(sk), phk, abort_flag)) ||
+              !uniform(mbar_wait(bar(kPBarP + 0), ph0, abort_flag)))
+            return false;
+        }
+        tc_fence_after();
+        gemm2(0, sv, true);
+        gemm1(0, dq[0], sk);
+        mma_commit_elect(bar(kPBarS + 0));
+        if (!uniform(mbar_try_wait(bar(kPBarP + 1), ph1))) {
+          if (!uniform(mbar_wait(bar(kPBarP + 1), ph1, abort_flag))) return false;
+        }
+        tc_fence_after();
+        gemm2(1, sv, true);
+        mma_commit_elect(empty(sv));
+        gemm1(1, dq[1], sk);
+        mma_commit_elect(bar(kPBarS + 1));
+        mma_commit_elect(empty(sk));
+        ++np[0];
+        ++np[1];
+        return true;
+      };
+      // first and last step of a unit
+      auto boundary = [&](int jj) -> bool {
+        const bool last = jj + 1 == cur.n_max;
+        const int iv = base_item + 2 * jj + 1, ik = iv + 1;
+        const int sv = iv % C::kRing, sk = ik % C::kRing;
+        const bool has_k = !last || has_nxt;
+        const bool pv0 = jj < cur.jhi[0], pv1 = jj < cur.jhi[1];
+        const bool sn0 = last ? (has_nxt && nxt.jhi[0] > 0) : (jj + 1 < cur.jhi[0]);
+        const bool sn1 = last ? (has_nxt && nxt.jhi[1] > 0) : (jj + 1 < cur.jhi[1]);
+        if (!uniform(mbar_wait(full(sv), (iv / C::kRing) & 1, abort_flag))) return false;
+        if (has_k && !uniform(mbar_wait(full(sk), (ik / C::kRing) & 1, abort_flag))) return false;
+        if (pv0 && !uniform(mbar_wait(bar(kPBarP + 0), np[0] & 1, abort_flag))) return false;
+        if (last) {
+          if (sn0 && !uniform(mbar_wait(bar(kPBarQFull + 2 * qb_n[0] + 0), (occ_n[0] / C::kQBufs) & 1, abort_flag))) return false;
+          if (sn1 && !uniform(mbar_wait(bar(kPBarQFull + 2 * qb_n[1] + 1), (occ_n[1] / C::kQBufs) & 1, abort_flag))) return false;
+        }
+        tc_fence_after();
+        if (pv0) {
+          ++np[0];
+          gemm2(0, sv, jj > 0);
+          if (jj == cur.jhi[0] - 1) mma_commit_elect(bar(kPBarOFinal + 0));
+        }
+        if (sn0) {
+          gemm1(0, last ? dq_n[0] : dq[0], sk);
+          mma_commit_elect(bar(kPBarS + 0));
+          if (last ? (nxt.jhi[0] == 1) : (jj + 2 == cur.jhi[0]))
+            mma_commit_elect(bar(kPBarQFree + 2 * (last ? qb_n[0] : qb[0]) + 0));
+        }
+        if (pv1) {
+          if (!uniform(mbar_wait(bar(kPBarP + 1), np[1] & 1, abort_flag))) return false;
+          ++np[1];
+          tc_fence_after();
+          gemm2(1, sv, jj > 0);
+          if (jj == cur.jhi[1] - 1) mma_commit_elect(bar(kPBarOFinal + 1));
+        }
+        mma_commit_elect(empty(sv));
+        if (sn1) {
+          gemm1(1, last ? dq_n[1] : dq[1], sk);
+          mma_commit_elect(bar(kPBarS + 1));
+          if (last ? (nxt.jhi[1] == 1) : (jj + 2 == cur.jhi[1]))
+            mma_commit_elect(bar(kPBarQFree + 2 * (last ? qb_n[1] : qb[1]) + 1));
+        }
+        if (has_k) mma_commit_elect(empty(sk));
+        return true;
+      };
+      if (unit_at(0, cur)) {
+        // prologue: the first unit's first S products
+        for (int t = 0; t < 2 && ok; ++t)
+          if (cur.jhi[t] > 0) ok = uniform(mbar_wait(bar(kPBarQFull + t), 0, abort_flag));
+        if (ok) ok = uniform(mbar_wait(full(0), 0, abort_flag));
+        if (ok) {
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (cur.jhi[t] > 0) {
+              gemm1(t, qdesc(0, t), 0);
+              mma_commit_elect(bar(kPBarS + t));
+              if (cur.jhi[t] == 1) mma_commit_elect(bar(kPBarQFree + t));
+            }
+          mma_commit_elect(empty(0));
+        }
+        for (int k = 0; ok; ++k) {
+          has_nxt = unit_at(k + 1, nxt);
+          for (int t = 0; t < 2; ++t) {
+            occ_n[t] = occ[t] + (cur.jhi[t] > 0 ? 1 : 0);
+            qb[t] = occ[t] % C::kQBufs;
+            qb_n[t] = occ_n[t] % C::kQBufs;
+            dq[t] = qdesc(qb[t], t);
+            dq_n[t] = qdesc(qb_n[t], t);
+          }
+          // steady range [1, s_hi): both tiles present, no last S or P V of either
+          int s_hi = 1;
+          if (cur.jhi[1] > 0) s_hi = max(1, min(cur.jhi[0], cur.jhi[1]) - 2);
+          const int n = cur.n_max;
+          ok = boundary(0);
+          int jj = 1;
+          for (; ok && jj < s_hi && jj < n - 1; ++jj) ok = steady(jj);
+          for (; ok && jj < n - 1; ++jj) ok = inner(jj);
+          if (ok && n > 1) ok = boundary(n - 1);
+          if (!ok || !has_nxt) break;
+          base_item += 2 * cur.n_max;
+          cur = nxt;
+          occ[0] = occ_n[0];
+          occ[1] = occ_n[1];
+        }
+      }
+      if (!ok) report_wait_failure(abort_flag, 4u);
+      // drain: every MMA issued so far has completed once this barrier flips
+      mma_commit_elect(bar(kPBarDrain));
+      uniform(mbar_wait(bar(kPBarDrain), 0, nullptr));
+    }
+  } else {
+    // ============== softmax, correction and epilogue (warps 0-7) =============
+    const int t = warp >> 2;
+    const int q = warp & 3;
+    const int row_local = q * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const uint32_t tS = lane_base + (t ? 128u : 0u);
+    const uint32_t tO = lane_base + C::kTmO + static_cast<uint32_t>(t * D);
+    const float c = p.scale_log2;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    int ns = 0;   // S phases consumed
+    int occ = 0;  // units in which this tile was present so far (O-final phases)
+    bool ok = true;
+    PUnit u;
+    for (int k = 0; ok && unit_at(k, u); ++k) {
+      const int nt = u.jhi[t];
+      if (nt == 0) continue;
+      const int row = u.row0[t] + row_local;
+      const int row_key_end = p.Nk;  // keys past Nk (the ragged last tile) are masked
+      float m_bar = NEG_INF;  // reference maximum, base-2 scaled units
+      float l = 0.f;
+      float r_max = NEG_INF;  // the row's largest score (raw units); see fa_fwd_kernel
+      for (int j = 0; j < nt; ++j) {
+        bool got = mbar_wait(bar(kPBarS + t), ns & 1, abort_flag);
+        ++ns;
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t s0[32], s1[32], s2[32], s3[32];
+        tmem_ld32(tS + 0, s0);
+        tmem_ld32(tS + 32, s1);
+        tmem_ld_wait(s0);
+        reg_pin(s1);
+        tmem_ld32(tS + 64, s2);
+        tmem_ld32(tS + 96, s3);
+        float* const f0 = reinterpret_cast<float*>(s0);
+        float* const f1 = reinterpret_cast<float*>(s1);
+        float* const f2 = reinterpret_cast<float*>(s2);
+        float* const f3 = reinterpret_cast<float*>(s3);
+        const int k0 = j * C::kBN;
+        const int lim_hi = min(C::kBN, max(0, row_key_end - k0));
+        const bool masked = lim_hi < C::kBN;
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (i >= lim_hi) f0[i] = NEG_INF;
+            if (32 + i >= lim_hi) f1[i] = NEG_INF;
+          }
+        }
+        float mx0 = fmax3(f0[0], f0[1], f1[0]), mx1 = fmax3(f0[2], f0[3], f1[1]);
+#pragma unroll
+        for (int i = 2; i < 16; ++i) {
+          if (i & 1) mx1 = fmax3(mx1, f0[2 * i], f0[2 * i + 1]);
+          else mx0 = fmax3(mx0, f0[2 * i], f0[2 * i + 1]);
+        }
+#pragma unroll
+        for (int i = 2; i < 32; i += 2) mx0 = fmax3(mx0, f1[i], f1[i + 1]);
+        tmem_ld_wait(s2);
+        reg_pin(s3);
+        if (masked) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (64 + i >= lim_hi) f2[i] = NEG_INF;
+            if (96 + i >= lim_hi) f3[i] = NEG_INF;
+          }
+        }
+        float mx2 = fmax3(f2[0], f2[1], f3[0]), mx3 = fmax3(f2[2], f2[3], f3[1]);
+#pragma unroll
+        for (int i = 2; i < 16; ++i) {
+          if (i & 1) mx3 = fmax3(mx3, f2[2 * i], f2[2 * i + 1]);
+          else mx2 = fmax3(mx2, f2[2 * i], f2[2 * i + 1]);
+        }
+#pragma unroll
+        for (int i = 2; i < 32; i += 2) mx2 = fmax3(mx2, f3[i], f3[i + 1]);
+        const float s_max = fmaxf(fmax3(mx0, mx1, mx2), mx3);
+        r_max = fmaxf(r_max, s_max);
+        const float m_new = s_max * c;
+        const bool need = m_new > m_bar + 8.0f;
+        const bool any_need = __any_sync(0xffffffffu, need);
+        float alpha = 1.0f;
+        if (need) {
+          alpha = ex2(m_bar - m_new);  // 0 on the first visible tile (m_bar = -inf)
+          m_bar = m_new;
+          l *= alpha;
+        }
+        const float neg_ref = (m_bar == NEG_INF) ? 0.f : -m_bar;
+        float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+        auto emit = [&](const float* f, uint32_t col) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            fma2(x0, x1, f[2 * i], f[2 * i + 1], c, neg_ref);
+            const float e0 = ex2(x0), e1 = ex2(x1);
+            if (i & 1) add2(ls2, ls3, e0, e1);
+            else add2(ls0, ls1, e0, e1);
+            pk[i] = pack_bf16(e0, e1);
+          }
+          tmem_st16(tS + col, pk);
+        };
+        emit(f0, 0);
+        emit(f1, 16);
+        emit(f2, 32);
+        emit(f3, 48);
+        l += (ls0 + ls1) + (ls2 + ls3);
+        // correction: O *= alpha for the rows whose reference moved (the
+        // previous P V of this tile has completed: S of this tile was issued
+        // after it and its commit covers it)
+        if (any_need && j > 0) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tO + cc * 32, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kPBarP + t));
+      }
+      if (!ok) break;
+      // ---- epilogue of this unit's tile: O / l to bf16, LSE --------------
+      bool got = mbar_wait(bar(kPBarOFinal + t), occ & 1, abort_flag);
+      ++occ;
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      // the row's largest P counted as rounded for P V (see fa_fwd_kernel)
+      float l_o = l;
+      if (l > 0.f) {
+        const float e_max = ex2(fmaf(r_max, c, -m_bar));
+        l_o += __uint_as_float(pack_bf16(e_max, 0.f) << 16) - e_max;
+      }
+      const float inv_l = (l > 0.f) ? (1.0f / l_o) : 0.f;
+      const bool store = row < p.Nq;
+      uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                   (static_cast<size_t>(u.bh) * p.Nq + row) * D);
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+        tmem_ld_wait(o);
+        if (store) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            orow[cc * 4 + i] = make_uint4(pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+                                          pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+                                          pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+                                          pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+        }
+      }
+      if (store)
+        p.lse[static_cast<size_t>(u.bh) * p.Nq + row] =
+            (l > 0.f) ? (m_bar + __log2f(l)) * 0.69314718055994530942f : NEG_INF;
+      // O has been read before this tile hands over its next P: the next
+      // unit's first P V (which overwrites O) cannot start earlier
+      tc_fence_before();
+    }
+    if (!ok) report_wait_failure(abort_flag, 1u);
+  }
+
+  // ---- teardown -----------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kWarpMma) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace fa

@@ -51,6 +51,16 @@ def test_window_flops_closed_forms():
     assert bench.flops_of(base.with_(causal=True)) == base.flops / 2
 
 
+def test_kernel_name_follows_dispatch():
+    w = synth.WORKLOADS["long_8192_d128"]
+    assert bench.kernel_name(w, None) == "fa_fwd_persist_kernel"
+    assert bench.kernel_name(w, 1) == "fa_fwd_persist_kernel"
+    assert bench.kernel_name(w, 4) == "fa_fwd_kernel"
+    assert bench.kernel_name(synth.WORKLOADS["long_8192_d128_causal"], None) == "fa_fwd_kernel"
+    assert bench.kernel_name(synth.WORKLOADS["single_head_4096_d64"], 1) == "fa_fwd_kernel"
+    assert bench.kernel_name(w.with_(window=(64, 0)), None) == "fa_fwd_kernel"
+
+
 def test_traffic_lookup(tmp_path, monkeypatch):
     h = bench.kernel_source_hash()
     f = tmp_path / "traffic.md"

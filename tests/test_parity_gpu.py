@@ -149,6 +149,20 @@ def test_many_short_heads(d, causal):
     _check_full(synth.Workload("many", 16, 128, 130, 130, d, causal, seed=40 + d + causal), 1)
 
 
+# the persistent d = 128 kernel (a single pass without a mask): more work units
+# than multiprocessors, so each CTA streams several units through one K/V ring
+# and one MMA stream; units whose second query tile is absent (Nq = 300: the
+# second pair holds one tile) or two rows long, key counts that are not tile
+# multiples, one key tile (S of the next unit issued in a unit's first step),
+# and fewer units than multiprocessors
+@pytest.mark.parametrize("shape", [(2, 80, 300, 1000), (1, 160, 256, 640), (3, 53, 130, 2000), (4, 40, 129, 100),
+                                   (1, 3, 1000, 4097)])
+def test_persistent_unit_stream(shape):
+    B, H, nq, nk = shape
+    _check_full(synth.Workload("persist", B, H, nq, nk, 128, False, seed=50 + H), 1)
+    _check_full(synth.Workload("persist_wide", B, H, nq, nk, 128, False, sigma_q=8.0, seed=60 + H))
+
+
 # --- degenerate and numerically hard cases -----------------------------------
 @pytest.mark.parametrize("d", [64, 128])
 def test_single_key(d):
