@@ -49,8 +49,19 @@ int g_dev_sms_or(int dev, int fallback) {
 }
 std::mutex g_dev_mutex;
 
+// A kernel that moves registers between warpgroups with setmaxnreg assumes
+// the register count it is launched with; with any other count an increase
+// could wait forever, so the library refuses such a build.
+template <typename K>
+bool launch_regs_are(K kernel, int regs) {
+  cudaFuncAttributes a;
+  return cudaFuncGetAttributes(&a, kernel) == cudaSuccess && a.numRegs == regs;
+}
+
 template <int D, int MASK, bool SPLIT, int TILES = 2>
 cudaError_t set_smem_attr() {
+  if (TILES == 2 && !launch_regs_are(fa::fa_fwd_kernel<D, MASK, SPLIT, TILES>, fa::Cfg<D, TILES>::kRegLaunch))
+    return cudaErrorInvalidDeviceFunction;
   return cudaFuncSetAttribute(fa::fa_fwd_kernel<D, MASK, SPLIT, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               static_cast<int>(fa::Cfg<D, TILES>::kSmemBytes));
 }
@@ -78,8 +89,9 @@ bool set_smem_attrs() {
             set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
   if constexpr (D == 128)
-    ok = ok && cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(fa::PCfg<128>::kSmemBytes)) == cudaSuccess;
+    ok = ok && launch_regs_are(fa::fa_fwd_persist_kernel<128>, fa::PCfg<128>::kRegLaunch) &&
+         cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fa::PCfg<128>::kSmemBytes)) == cudaSuccess;
   if constexpr (D == 64)
     ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess &&
          set_smem_attr<64, fa::kMaskNone, true, 1>() == cudaSuccess &&

@@ -17,13 +17,17 @@
 // "pinghaoyang FlashAttention 1-4 guide", FA4 section); the final division
 // by the true normaliser keeps the result exact.  S and P never leave the SM.
 //
-// GB300 mapping (one CTA per SM, 320 threads):
+// GB300 mapping (one CTA per SM, 384 threads):
 //   warps 0-3  softmax + correction + epilogue for query tile 0 (TMEM lanes 0-127)
 //   warps 4-7  the same for query tile 1
 //   warp  8    TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... through
 //              one ring of kRing tile-sized slots (mbarrier full/empty per slot)
 //   warp  9    MMA issuer: the whole warp runs the loop, one elected lane
 //              issues every tcgen05.mma and commit to mbarriers
+//   warps 10-11 idle: they complete warpgroup 2 (warps 8-11), which hands
+//              registers to the softmax warpgroups with setmaxnreg (168 at
+//              launch; 184 for warps 0-7, 128 for warps 8-11), so that the
+//              128-float S row and the loop state fit without spilling
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D);
 //   P_i (bf16, packed in pairs) overwrites the first 64 columns of S_i and is
@@ -80,7 +84,15 @@ struct Cfg {
   static_assert(TILES == 2 || (TILES == 1 && D == 64), "query tiles per CTA");
   static constexpr int kTiles = TILES;
   static constexpr int kWarpProd = 4 * kTiles, kWarpMma = 4 * kTiles + 1;
-  static constexpr int kThreads = 32 * (4 * kTiles + 2);
+  // two query tiles: 12 warps (softmax 0-7, producer 8, MMA 9, idle 10-11),
+  // so that warps 8-11 form a whole warpgroup whose registers setmaxnreg
+  // moves to the softmax warpgroups; one tile: 6 warps, no register move
+  static constexpr int kThreads = (kTiles == 2) ? 384 : 32 * (4 * kTiles + 2);
+  static constexpr int kRegLaunch = 168;   // what ptxas gives 384 threads at one CTA per SM (checked by the host)
+  static constexpr int kRegSoftmax = 184;  // warpgroups 0 and 1
+  static constexpr int kRegMisc = 128;     // warpgroup 2
+  static_assert(kTiles == 1 || 2 * 128 * kRegSoftmax + 128 * kRegMisc <= kThreads * kRegLaunch, "register split");
+  static_assert(kRegMisc <= kRegLaunch && kRegSoftmax >= kRegLaunch, "setmaxnreg direction");
   static constexpr int kMinBlocks = (kTiles == 1) ? 2 : 1;  // CTAs per SM
   static constexpr int kBM = 128;  // query rows per tile (MMA M)
   static constexpr int kBN = 128;  // keys per tile
@@ -241,215 +253,221 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
   }
   const int n_items = 2 * n_max;  // ring items: K_j = item 2j, V_j = item 2j+1
 
-  if (warp == C::kWarpProd) {
-    // ======================= TMA producer =================================
-    // d = 64: the whole warp runs the loop (each barrier outcome made uniform
-    // with a vote) and one lane chosen by elect.sync issues every expect-tx
-    // and copy, as in the MMA issuer below.  A d = 64 K/V tile carries half
-    // the MMA work of a d = 128 one, so the producer's issue latency weighs
-    // twice as much there.  d = 128: lane 0 alone.
-    auto uniform = [](bool v) -> bool {
-      if constexpr (D == 64) return __all_sync(0xffffffffu, v);
-      else return v;
-    };
-    auto expect_tx = [](uint32_t b, uint32_t bytes) {
-      if constexpr (D == 64) mbar_arrive_expect_tx_elect(b, bytes);
-      else mbar_arrive_expect_tx(b, bytes);
-    };
-    auto load = [](uint32_t dst, const CUtensorMap* map, uint32_t b, int x, int y, int z) {
-      if constexpr (D == 64) tma_load_3d_elect(dst, map, b, x, y, z);
-      else tma_load_3d(dst, map, b, x, y, z);
-    };
-    if (D == 64 || lane == 0) {
-      tma_prefetch_map(&tmQ);
-      tma_prefetch_map(&tmK);
-      tma_prefetch_map(&tmV);
-      tma_prefetch_map(&tmO);
-      for (int t = 0; t < 2; ++t) {
-        if (nkv[t] == 0) continue;
-        const uint32_t dst = base + C::kQOff + t * C::kTileBytes;
-        expect_tx(bar(kBarQ + t), C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b)
-          load(dst + b * C::kBoxBytes, &tmQ, bar(kBarQ + t), b * 64, row0[t], bh);
-      }
-      int issued = 0;
-      for (int item = 0; item < n_items; ++item) {
-        const int s = item % C::kRing;
-        const uint32_t ph = (item / C::kRing) & 1;
-        if (!uniform(mbar_wait(empty(s), ph ^ 1u, abort_flag))) {
-          report_wait_failure(abort_flag, 2u);
-          break;
+  if (warp >= 4 * TILES) {
+    // warpgroup 2 (producer, MMA issuer and, with two tiles, two idle warps)
+    // gives registers to the softmax warpgroups
+    if constexpr (TILES == 2) regs_dec<C::kRegMisc>();
+    if (warp == C::kWarpProd) {
+      // ======================= TMA producer =================================
+      // d = 64: the whole warp runs the loop (each barrier outcome made uniform
+      // with a vote) and one lane chosen by elect.sync issues every expect-tx
+      // and copy, as in the MMA issuer below.  A d = 64 K/V tile carries half
+      // the MMA work of a d = 128 one, so the producer's issue latency weighs
+      // twice as much there.  d = 128: lane 0 alone.
+      auto uniform = [](bool v) -> bool {
+        if constexpr (D == 64) return __all_sync(0xffffffffu, v);
+        else return v;
+      };
+      auto expect_tx = [](uint32_t b, uint32_t bytes) {
+        if constexpr (D == 64) mbar_arrive_expect_tx_elect(b, bytes);
+        else mbar_arrive_expect_tx(b, bytes);
+      };
+      auto load = [](uint32_t dst, const CUtensorMap* map, uint32_t b, int x, int y, int z) {
+        if constexpr (D == 64) tma_load_3d_elect(dst, map, b, x, y, z);
+        else tma_load_3d(dst, map, b, x, y, z);
+      };
+      if (D == 64 || lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+        tma_prefetch_map(&tmO);
+        for (int t = 0; t < 2; ++t) {
+          if (nkv[t] == 0) continue;
+          const uint32_t dst = base + C::kQOff + t * C::kTileBytes;
+          expect_tx(bar(kBarQ + t), C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            load(dst + b * C::kBoxBytes, &tmQ, bar(kBarQ + t), b * 64, row0[t], bh);
         }
-        const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
-        expect_tx(full(s), C::kTileBytes);
-        for (int b = 0; b < C::kBoxes; ++b)
-          load(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (J0 + (item >> 1)) * C::kBN, bh);
-        issued = item + 1;
-      }
-      if (*abort_flag) {
-        // Let every copy already issued land before the CTA can exit: the
-        // last item issued into each slot is among the final kRing items.
-        for (int item = max(0, issued - C::kRing); item < issued; ++item)
-          uniform(mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, nullptr));
-        for (int t = 0; t < 2; ++t)
-          if (nkv[t] > 0) uniform(mbar_wait(bar(kBarQ + t), 0, nullptr));
-      }
-    }
-  } else if (warp == C::kWarpMma) {
-    // ======================= MMA issuer ====================================
-    // The whole warp runs the issue loop on warp-uniform values (every
-    // barrier outcome made uniform with a vote); one lane chosen by
-    // elect.sync issues each tcgen05.mma and commit, with no branch around the
-    // instruction.  Same-box A/B against lane 0 alone: +4% to +7.5% at d = 64,
-    // and at d = 128 +1% together with the branch-free steady body below.
-    auto mma_ss_x = [](uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
-      mma_ss_elect(d_tmem, a_desc, b_desc, idesc, acc);
-    };
-    auto mma_ts_x = [](uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
-      mma_ts_elect(d_tmem, a_tmem, b_desc, idesc, acc);
-    };
-    auto commit_x = [](uint32_t b) { mma_commit_elect(b); };
-    auto uniform = [](bool v) -> bool { return __all_sync(0xffffffffu, v); };
-    {
-      // descriptors: start address lives in bits 0-13 (address >> 4), so a
-      // byte offset is added to a base descriptor as (offset >> 4)
-      const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
-      const uint64_t dQ1 = sdesc_sw128(base + C::kQOff + C::kTileBytes, 16, 1024);
-      const uint64_t dK0 = sdesc_sw128(base + C::kRingOff, 16, 1024);
-      const uint64_t dV0 = sdesc_sw128(base + C::kRingOff, C::kBoxBytes, 1024);
-      const uint32_t tS[2] = {tmem + C::kTmS0, tmem + C::kTmS1};
-      const uint32_t tO[2] = {tmem + C::kTmO0, tmem + C::kTmO1};
-      auto gemm1 = [&](int t, int slot) {
-        const uint64_t dq = t ? dQ1 : dQ0;
-        const uint64_t dk = dK0 + ((slot * C::kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
-          mma_ss_x(tS[t], dq + off, dk + off, C::kIdescS, kk > 0 ? 1u : 0u);
-        }
-      };
-      auto gemm2 = [&](int t, int slot, bool acc_prev) {
-        const uint64_t dv = dV0 + ((slot * C::kTileBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < C::kBN / 16; ++kk)
-          mma_ts_x(tO[t], tS[t] + kk * 8, dv + ((kk * 2048) >> 4), C::kIdescO, (acc_prev || kk > 0) ? 1u : 0u);
-      };
-      auto wait_item = [&](int item) -> bool {
-        return uniform(mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, abort_flag));
-      };
-      auto uwait = [&](uint32_t b, uint32_t ph) -> bool { return uniform(mbar_wait(b, ph, abort_flag)); };
-      // is K/V tile j (absolute index within the head) visible to query tile t?
-      auto in_range = [&](int t, int j) -> bool { return j >= jlo[t] && j < jhi[t]; };
-      bool ok = true;
-      for (int t = 0; t < 2 && ok; ++t)
-        if (nkv[t] > 0) ok = uwait(bar(kBarQ + t), 0);
-      if (ok && n_max > 0) ok = wait_item(0);
-      if (ok && n_max > 0) {
-        tc_fence_after();
-        for (int t = 0; t < 2; ++t)
-          if (nkv[t] > 0 && jlo[t] == J0) {
-            gemm1(t, 0);
-            commit_x(bar(kBarS + t));
+        int issued = 0;
+        for (int item = 0; item < n_items; ++item) {
+          const int s = item % C::kRing;
+          const uint32_t ph = (item / C::kRing) & 1;
+          if (!uniform(mbar_wait(empty(s), ph ^ 1u, abort_flag))) {
+            report_wait_failure(abort_flag, 2u);
+            break;
           }
-        commit_x(empty(0));
+          const CUtensorMap* map = (item & 1) ? &tmV : &tmK;
+          expect_tx(full(s), C::kTileBytes);
+          for (int b = 0; b < C::kBoxes; ++b)
+            load(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (J0 + (item >> 1)) * C::kBN, bh);
+          issued = item + 1;
+        }
+        if (*abort_flag) {
+          // Let every copy already issued land before the CTA can exit: the
+          // last item issued into each slot is among the final kRing items.
+          for (int item = max(0, issued - C::kRing); item < issued; ++item)
+            uniform(mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, nullptr));
+          for (int t = 0; t < 2; ++t)
+            if (nkv[t] > 0) uniform(mbar_wait(bar(kBarQ + t), 0, nullptr));
+        }
       }
-      // Issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), with
-      // every barrier check of the first half gathered in one place (each
-      // check behind queued MMAs costs a pipe bubble, consecutive ones cost one).
-      // A tile whose range starts after J0 gets its first S when j + 1 enters it.
-      auto general = [&](int jj) -> bool {
-        const int j = J0 + jj;
-        const int iv = 2 * jj + 1, ik = 2 * jj + 2;  // ring items of V_j and K_{j+1}
-        const int sv = iv % C::kRing, sk = ik % C::kRing;
-        const bool has_next = (jj + 1) < n_max;
-        const bool pv0 = in_range(0, j), pv1 = in_range(1, j);
-        {
-          // the three checks are issued back to back so their latencies overlap
-          const bool a = mbar_try_wait(full(sv), (iv / C::kRing) & 1);
-          const bool b = !has_next || mbar_try_wait(full(sk), (ik / C::kRing) & 1);
-          const bool c = !pv0 || mbar_try_wait(bar(kBarP + 0), (j - jlo[0]) & 1);
+    } else if (warp == C::kWarpMma) {
+      // ======================= MMA issuer ====================================
+      // The whole warp runs the issue loop on warp-uniform values (every
+      // barrier outcome made uniform with a vote); one lane chosen by
+      // elect.sync issues each tcgen05.mma and commit, with no branch around the
+      // instruction.  Same-box A/B against lane 0 alone: +4% to +7.5% at d = 64,
+      // and at d = 128 +1% together with the branch-free steady body below.
+      auto mma_ss_x = [](uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+        mma_ss_elect(d_tmem, a_desc, b_desc, idesc, acc);
+      };
+      auto mma_ts_x = [](uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc, uint32_t acc) {
+        mma_ts_elect(d_tmem, a_tmem, b_desc, idesc, acc);
+      };
+      auto commit_x = [](uint32_t b) { mma_commit_elect(b); };
+      auto uniform = [](bool v) -> bool { return __all_sync(0xffffffffu, v); };
+      {
+        // descriptors: start address lives in bits 0-13 (address >> 4), so a
+        // byte offset is added to a base descriptor as (offset >> 4)
+        const uint64_t dQ0 = sdesc_sw128(base + C::kQOff, 16, 1024);
+        const uint64_t dQ1 = sdesc_sw128(base + C::kQOff + C::kTileBytes, 16, 1024);
+        const uint64_t dK0 = sdesc_sw128(base + C::kRingOff, 16, 1024);
+        const uint64_t dV0 = sdesc_sw128(base + C::kRingOff, C::kBoxBytes, 1024);
+        const uint32_t tS[2] = {tmem + C::kTmS0, tmem + C::kTmS1};
+        const uint32_t tO[2] = {tmem + C::kTmO0, tmem + C::kTmO1};
+        auto gemm1 = [&](int t, int slot) {
+          const uint64_t dq = t ? dQ1 : dQ0;
+          const uint64_t dk = dK0 + ((slot * C::kTileBytes) >> 4);
+  #pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * C::kBoxBytes + (kk & 3) * 32) >> 4;
+            mma_ss_x(tS[t], dq + off, dk + off, C::kIdescS, kk > 0 ? 1u : 0u);
+          }
+        };
+        auto gemm2 = [&](int t, int slot, bool acc_prev) {
+          const uint64_t dv = dV0 + ((slot * C::kTileBytes) >> 4);
+  #pragma unroll
+          for (int kk = 0; kk < C::kBN / 16; ++kk)
+            mma_ts_x(tO[t], tS[t] + kk * 8, dv + ((kk * 2048) >> 4), C::kIdescO, (acc_prev || kk > 0) ? 1u : 0u);
+        };
+        auto wait_item = [&](int item) -> bool {
+          return uniform(mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, abort_flag));
+        };
+        auto uwait = [&](uint32_t b, uint32_t ph) -> bool { return uniform(mbar_wait(b, ph, abort_flag)); };
+        // is K/V tile j (absolute index within the head) visible to query tile t?
+        auto in_range = [&](int t, int j) -> bool { return j >= jlo[t] && j < jhi[t]; };
+        bool ok = true;
+        for (int t = 0; t < 2 && ok; ++t)
+          if (nkv[t] > 0) ok = uwait(bar(kBarQ + t), 0);
+        if (ok && n_max > 0) ok = wait_item(0);
+        if (ok && n_max > 0) {
+          tc_fence_after();
+          for (int t = 0; t < 2; ++t)
+            if (nkv[t] > 0 && jlo[t] == J0) {
+              gemm1(t, 0);
+              commit_x(bar(kBarS + t));
+            }
+          commit_x(empty(0));
+        }
+        // Issue order per K/V tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), with
+        // every barrier check of the first half gathered in one place (each
+        // check behind queued MMAs costs a pipe bubble, consecutive ones cost one).
+        // A tile whose range starts after J0 gets its first S when j + 1 enters it.
+        auto general = [&](int jj) -> bool {
+          const int j = J0 + jj;
+          const int iv = 2 * jj + 1, ik = 2 * jj + 2;  // ring items of V_j and K_{j+1}
+          const int sv = iv % C::kRing, sk = ik % C::kRing;
+          const bool has_next = (jj + 1) < n_max;
+          const bool pv0 = in_range(0, j), pv1 = in_range(1, j);
+          {
+            // the three checks are issued back to back so their latencies overlap
+            const bool a = mbar_try_wait(full(sv), (iv / C::kRing) & 1);
+            const bool b = !has_next || mbar_try_wait(full(sk), (ik / C::kRing) & 1);
+            const bool c = !pv0 || mbar_try_wait(bar(kBarP + 0), (j - jlo[0]) & 1);
+            if (!uniform(a && b && c)) {
+              if (!wait_item(iv)) return false;
+              if (has_next && !wait_item(ik)) return false;
+              if (pv0 && !uwait(bar(kBarP + 0), (j - jlo[0]) & 1)) return false;
+            }
+          }
+          tc_fence_after();
+          if (pv0) {
+            gemm2(0, sv, j > jlo[0]);
+            if (j == jhi[0] - 1) commit_x(bar(kBarO + 0));
+          }
+          if (has_next && in_range(0, j + 1)) {
+            gemm1(0, sk);
+            commit_x(bar(kBarS + 0));
+          }
+          if (pv1) {
+            if (!uwait(bar(kBarP + 1), (j - jlo[1]) & 1)) return false;
+            tc_fence_after();
+            gemm2(1, sv, j > jlo[1]);
+            if (j == jhi[1] - 1) commit_x(bar(kBarO + 1));
+          }
+          commit_x(empty(sv));
+          if (has_next && in_range(1, j + 1)) {
+            gemm1(1, sk);
+            commit_x(bar(kBarS + 1));
+          }
+          if (has_next) commit_x(empty(sk));
+          return true;
+        };
+        // The steady state: K/V tiles j with j - 1, j and j + 1 in both query
+        // tiles' ranges, so every product of the tile is issued and none is the
+        // last of its tile.  The same issue order without a branch around the
+        // MMAs: a barrier test by this thread completes only after its queued
+        // MMAs, and a branch next to it costs the pipe about 20 cycles per MMA.
+        auto steady = [&](int jj) -> bool {
+          const int j = J0 + jj;
+          const int iv = 2 * jj + 1, ik = 2 * jj + 2;
+          const int sv = iv % C::kRing, sk = ik % C::kRing;
+          const uint32_t phv = (iv / C::kRing) & 1, phk = (ik / C::kRing) & 1;
+          const uint32_t ph0 = (j - jlo[0]) & 1, ph1 = (j - jlo[1]) & 1;
+          const bool a = mbar_try_wait(full(sv), phv);
+          const bool b = mbar_try_wait(full(sk), phk);
+          const bool c = mbar_try_wait(bar(kBarP + 0), ph0);
           if (!uniform(a && b && c)) {
-            if (!wait_item(iv)) return false;
-            if (has_next && !wait_item(ik)) return false;
-            if (pv0 && !uwait(bar(kBarP + 0), (j - jlo[0]) & 1)) return false;
+            if (!uwait(full(sv), phv) || !uwait(full(sk), phk) || !uwait(bar(kBarP + 0), ph0)) return false;
           }
-        }
-        tc_fence_after();
-        if (pv0) {
-          gemm2(0, sv, j > jlo[0]);
-          if (j == jhi[0] - 1) commit_x(bar(kBarO + 0));
-        }
-        if (has_next && in_range(0, j + 1)) {
+          tc_fence_after();
+          gemm2(0, sv, true);
           gemm1(0, sk);
           commit_x(bar(kBarS + 0));
-        }
-        if (pv1) {
-          if (!uwait(bar(kBarP + 1), (j - jlo[1]) & 1)) return false;
+          if (!uniform(mbar_try_wait(bar(kBarP + 1), ph1))) {
+            if (!uwait(bar(kBarP + 1), ph1)) return false;
+          }
           tc_fence_after();
-          gemm2(1, sv, j > jlo[1]);
-          if (j == jhi[1] - 1) commit_x(bar(kBarO + 1));
-        }
-        commit_x(empty(sv));
-        if (has_next && in_range(1, j + 1)) {
+          gemm2(1, sv, true);
+          commit_x(empty(sv));
           gemm1(1, sk);
           commit_x(bar(kBarS + 1));
+          commit_x(empty(sk));
+          return true;
+        };
+        // steady range [s_lo, s_hi) of jj; the tiles before and after it take
+        // the general body.  With the elected issue it gains at both head sizes
+        // (with lane 0 alone it had measured 3% slower at d = 128).
+        int s_lo = n_max, s_hi = n_max;
+        if (nkv[0] > 0 && nkv[1] > 0) {
+          const int lo = max(jlo[0], jlo[1]) + 1 - J0, hi = min(jhi[0], jhi[1]) - 1 - J0;
+          if (lo < hi) {
+            s_lo = lo;
+            s_hi = hi;
+          }
         }
-        if (has_next) commit_x(empty(sk));
-        return true;
-      };
-      // The steady state: K/V tiles j with j - 1, j and j + 1 in both query
-      // tiles' ranges, so every product of the tile is issued and none is the
-      // last of its tile.  The same issue order without a branch around the
-      // MMAs: a barrier test by this thread completes only after its queued
-      // MMAs, and a branch next to it costs the pipe about 20 cycles per MMA.
-      auto steady = [&](int jj) -> bool {
-        const int j = J0 + jj;
-        const int iv = 2 * jj + 1, ik = 2 * jj + 2;
-        const int sv = iv % C::kRing, sk = ik % C::kRing;
-        const uint32_t phv = (iv / C::kRing) & 1, phk = (ik / C::kRing) & 1;
-        const uint32_t ph0 = (j - jlo[0]) & 1, ph1 = (j - jlo[1]) & 1;
-        const bool a = mbar_try_wait(full(sv), phv);
-        const bool b = mbar_try_wait(full(sk), phk);
-        const bool c = mbar_try_wait(bar(kBarP + 0), ph0);
-        if (!uniform(a && b && c)) {
-          if (!uwait(full(sv), phv) || !uwait(full(sk), phk) || !uwait(bar(kBarP + 0), ph0)) return false;
-        }
-        tc_fence_after();
-        gemm2(0, sv, true);
-        gemm1(0, sk);
-        commit_x(bar(kBarS + 0));
-        if (!uniform(mbar_try_wait(bar(kBarP + 1), ph1))) {
-          if (!uwait(bar(kBarP + 1), ph1)) return false;
-        }
-        tc_fence_after();
-        gemm2(1, sv, true);
-        commit_x(empty(sv));
-        gemm1(1, sk);
-        commit_x(bar(kBarS + 1));
-        commit_x(empty(sk));
-        return true;
-      };
-      // steady range [s_lo, s_hi) of jj; the tiles before and after it take
-      // the general body.  With the elected issue it gains at both head sizes
-      // (with lane 0 alone it had measured 3% slower at d = 128).
-      int s_lo = n_max, s_hi = n_max;
-      if (nkv[0] > 0 && nkv[1] > 0) {
-        const int lo = max(jlo[0], jlo[1]) + 1 - J0, hi = min(jhi[0], jhi[1]) - 1 - J0;
-        if (lo < hi) {
-          s_lo = lo;
-          s_hi = hi;
-        }
+        int jj = 0;
+        for (; ok && jj < s_lo; ++jj) ok = general(jj);
+        for (; ok && jj < s_hi; ++jj) ok = steady(jj);
+        for (; ok && jj < n_max; ++jj) ok = general(jj);
+        if (!ok) report_wait_failure(abort_flag, 4u);
+        // Drain: every MMA issued so far has completed once this barrier flips.
+        commit_x(bar(kBarDrain));
+        mbar_wait(bar(kBarDrain), 0, nullptr);
       }
-      int jj = 0;
-      for (; ok && jj < s_lo; ++jj) ok = general(jj);
-      for (; ok && jj < s_hi; ++jj) ok = steady(jj);
-      for (; ok && jj < n_max; ++jj) ok = general(jj);
-      if (!ok) report_wait_failure(abort_flag, 4u);
-      // Drain: every MMA issued so far has completed once this barrier flips.
-      commit_x(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, nullptr);
     }
   } else {
+    if constexpr (TILES == 2) regs_inc<C::kRegSoftmax>();
     // ============== softmax / correction / epilogue (warps 0-7) ===========
     const int t = warp >> 2;        // query tile of this warpgroup
     const int wq = warp & 3;        // TMEM lane quarter

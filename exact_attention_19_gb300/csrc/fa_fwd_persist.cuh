@@ -14,7 +14,8 @@
 //    first S products where it would otherwise compute the next tile's, so
 //    the tensor pipe sees no start or end of a unit, and no CTA is launched,
 //    set up or torn down per unit.
-//  * 12 warps, every one with the same 168 registers:
+//  * 12 warps, launched with 168 registers each; setmaxnreg then gives
+//    warps 0-7 184 and warps 8-11 128 (as in fa_fwd_kernel):
 //      warps 0-3   softmax, conditional rescale and epilogue of query tile 0
 //      warps 4-7   the same for query tile 1
 //      warp  8     TMA producer of the K/V ring
@@ -48,7 +49,7 @@ namespace fa {
 template <int D>
 struct PCfg {
   static_assert(D == 128, "the persistent schedule is built for d = 128 only");
-  static constexpr int kThreads = 384;  // three warpgroups: the registers of 10 warps' worth are allocated anyway
+  static constexpr int kThreads = 384;  // three warpgroups
   static constexpr int kWarpKV = 8, kWarpMma = 9, kWarpQ = 10;
   static constexpr int kBM = 128, kBN = 128;
   static constexpr int kQBufs = 1;  // Q buffers per query tile
@@ -65,6 +66,9 @@ struct PCfg {
   static constexpr uint32_t kTmO = 256;  // O[t] at kTmO + t * D
   static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
   static constexpr uint32_t kIdescO = idesc_bf16(128, D, true);
+  // registers per thread: at launch (checked by the host), softmax warpgroups, warpgroup 2
+  static constexpr int kRegLaunch = 168, kRegSoftmax = 184, kRegMisc = 128;
+  static_assert(2 * 128 * kRegSoftmax + 128 * kRegMisc <= kThreads * kRegLaunch, "register split");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -169,6 +173,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
   };
 
   if (warp >= 8) {
+    regs_dec<C::kRegMisc>();
     if (warp == C::kWarpKV && lane == 0) {
       // ======================= K/V producer ===============================
       tma_prefetch_map(&tmK);
@@ -438,6 +443,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       uniform(mbar_wait(bar(kPBarDrain), 0, nullptr));
     }
   } else {
+    regs_inc<C::kRegSoftmax>();
     // ============== softmax, correction and epilogue (warps 0-7) =============
     const int t = warp >> 2;
     const int q = warp & 3;

@@ -87,6 +87,20 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// setmaxnreg: every warp of a warpgroup executes the same one.  An increase
+// draws on the registers the CTA was launched with, which the decreases of
+// the other warpgroups have released.
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // Elected forms of the producer's expect-tx and tile load: executed by a whole
 // converged warp, performed by its one elected lane.
 __device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {

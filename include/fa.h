@@ -77,8 +77,11 @@ typedef enum {
  * Errors: argument problems return a code before anything is launched and
  * nothing is written.  Nq == 0 is a successful no-op; q, o and lse may then be
  * NULL (k and v may not).  FA_ERR_LAUNCH is
- * returned if the launch itself fails; faults during execution surface, as
- * usual for CUDA, at the next synchronising call on the stream.
+ * returned if the launch itself fails, and by every call of a build whose
+ * forward kernels did not get the register count their warpgroup register
+ * split assumes (checked once per device, before any launch); faults during
+ * execution surface, as usual for CUDA, at the next synchronising call on
+ * the stream.
  */
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
            int Nk, int d, float scale, int causal, cudaStream_t stream);
