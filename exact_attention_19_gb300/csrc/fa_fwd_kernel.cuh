@@ -26,8 +26,9 @@
 //              issues every tcgen05.mma and commit to mbarriers
 //   warps 10-11 idle: they complete warpgroup 2 (warps 8-11), which hands
 //              registers to the softmax warpgroups with setmaxnreg (168 at
-//              launch; 184 for warps 0-7, 128 for warps 8-11), so that the
-//              128-float S row and the loop state fit without spilling
+//              launch; then 184 for warps 0-7 and 128 for warps 8-11, or
+//              192 and 120 at d = 64, whose MMA issuer needs fewer), so that
+//              the 128-float S row and the loop state fit without spilling
 // TMEM (512 columns x 128 lanes x 32 bit):
 //   S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D, 256+2D);
 //   P_i (bf16, packed in pairs) overwrites the first 64 columns of S_i and is
@@ -89,8 +90,8 @@ struct Cfg {
   // moves to the softmax warpgroups; one tile: 6 warps, no register move
   static constexpr int kThreads = (kTiles == 2) ? 384 : 32 * (4 * kTiles + 2);
   static constexpr int kRegLaunch = 168;   // what ptxas gives 384 threads at one CTA per SM (checked by the host)
-  static constexpr int kRegSoftmax = 184;  // warpgroups 0 and 1
-  static constexpr int kRegMisc = 128;     // warpgroup 2
+  static constexpr int kRegSoftmax = (D == 64) ? 192 : 184;  // warpgroups 0 and 1
+  static constexpr int kRegMisc = (D == 64) ? 120 : 128;     // warpgroup 2
   static_assert(kTiles == 1 || 2 * 128 * kRegSoftmax + 128 * kRegMisc <= kThreads * kRegLaunch, "register split");
   static_assert(kRegMisc <= kRegLaunch && kRegSoftmax >= kRegLaunch, "setmaxnreg direction");
   static constexpr int kMinBlocks = (kTiles == 1) ? 2 : 1;  // CTAs per SM

@@ -453,6 +453,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     const uint32_t tO = lane_base + C::kTmO + static_cast<uint32_t>(t * D);
     const float c = p.scale_log2;
     const float NEG_INF = -__int_as_float(0x7f800000);
+    const bool o_aligned32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;
     int ns = 0;   // S phases consumed
     int occ = 0;  // units in which this tile was present so far (O-final phases)
     bool ok = true;
@@ -587,20 +588,33 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       }
       const float inv_l = (l > 0.f) ? (1.0f / l_o) : 0.f;
       const bool store = row < p.Nq;
-      uint4* const orow = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                                   (static_cast<size_t>(u.bh) * p.Nq + row) * D);
+      uint16_t* const orow = static_cast<uint16_t*>(p.o) + (static_cast<size_t>(u.bh) * p.Nq + row) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(tO + cc * 32, o);
         tmem_ld_wait(o);
         if (store) {
+          // a row is D * 2 = 256 bytes from a 256-byte multiple: with a 32-byte
+          // aligned O every store fills whole sectors
+          if (o_aligned32) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            orow[cc * 4 + i] = make_uint4(pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+            for (int h = 0; h < 2; ++h) {
+              uint32_t w[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                w[i] = pack_bf16(__uint_as_float(o[16 * h + 2 * i]) * inv_l, __uint_as_float(o[16 * h + 2 * i + 1]) * inv_l);
+              st_global_v8(orow + cc * 32 + h * 16, w);
+            }
+          } else {
+            uint4* const o4 = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              o4[cc * 4 + i] = make_uint4(pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
                                           pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
                                           pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
                                           pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+          }
         }
       }
       if (store)

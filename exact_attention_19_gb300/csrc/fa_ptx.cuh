@@ -121,6 +121,14 @@ __device__ __forceinline__ void tma_load_3d_elect(uint32_t dst, const CUtensorMa
       : "memory");
 }
 
+// 32-byte global store of eight 32-bit words (one whole sector); the address
+// must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&r)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(r[0]), "r"(r[1]),
+               "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 // Tiled TMA store shared -> global, completion tracked by bulk groups.  x must
 // be a multiple of 8 for bf16 and no coordinate may be negative; elements of
 // the box outside the tensor are not written.

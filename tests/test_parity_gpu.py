@@ -241,15 +241,17 @@ def test_deterministic():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-@pytest.mark.parametrize("mode", ["causal_d128", "full_d128", "causal_d64_single_tile", "full_d64", "window_d128",
-                                  "split_d64", "split_causal_d128"])
+@pytest.mark.parametrize("mode", ["causal_d128", "full_d128", "full_d128_o16", "causal_d64_single_tile", "full_d64",
+                                  "window_d128", "split_d64", "split_causal_d128"])
 def test_outputs_not_written_outside(mode):
     """O and LSE embedded in larger guard-filled buffers: the guards stay untouched.
 
     O goes out through tiled tensor stores of whole 128-row tiles; the last
     tile of every head here is ragged (333 rows), so the stores must drop the
     rows past Nq of the last head (past the buffer) and of every other head
-    (the next head's rows).  Covers each kernel instantiation's epilogue."""
+    (the next head's rows).  Covers each kernel instantiation's epilogue.
+    full_d128_o16 places O 16 bytes off a 32-byte boundary: the persistent
+    kernel's 32-byte row stores must give way to 16-byte ones there."""
     import torch
 
     import exact_attention_19_gb300 as fa
@@ -261,7 +263,7 @@ def test_outputs_not_written_outside(mode):
     q, k, v = w.make()
     tq, tk, tv = to_device(q), to_device(k), to_device(v)
     n_o, n_l = q.size, B * H * N
-    pad_o, pad_l = 4096, 64
+    pad_o, pad_l = (4096 + 8 if mode.endswith("o16") else 4096), 64  # 8 bf16 = 16 bytes
     big_o = torch.full((n_o + 2 * pad_o,), 7.0, dtype=torch.bfloat16, device="cuda")
     big_l = torch.full((n_l + 2 * pad_l,), -3.0, dtype=torch.float32, device="cuda")
     o = big_o[pad_o:pad_o + n_o].view(q.shape)
