@@ -473,7 +473,12 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
     const int t = warp >> 2;        // query tile of this warpgroup
     const int wq = warp & 3;        // TMEM lane quarter
     const int row_local = wq * 32 + lane;
-    const int row = row0[t] + row_local;
+    // this tile's values by select, not by a runtime index (which would put
+    // the arrays in local memory and reload them inside the loop)
+    const int row0_t = t ? row0[1] : row0[0];
+    const int key0_t = (t ? jlo[1] : jlo[0]) * C::kBN;  // first key of the tile's first K/V tile
+    const int nkv_t = t ? nkv[1] : nkv[0];
+    const int row = row0_t + row_local;
     // keys [row_key_lo, row_key_end) are visible to this row; all sizes fit
     // an int (N < 2^31), the window bounds are clamped into [-1, Nk]
     int row_key_lo = 0, row_key_end = p.Nk;
@@ -498,7 +503,7 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
     // recompute that P bit for bit.
     float r_max = NEG_INF;
     bool ok = true;
-    const int nt = nkv[t];
+    const int nt = nkv_t;
     for (int j = 0; j < nt; ++j) {
       bool got = mbar_wait(bar(kBarS + t), j & 1, abort_flag);
       got = __all_sync(0xffffffffu, got);
@@ -520,7 +525,7 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
 
       // masking: columns outside [lim_lo, lim_hi) of this K/V tile are not
       // visible to this row (window / causal bounds, ragged key tail)
-      const int k0 = (jlo[t] + j) * C::kBN;  // first key of this K/V tile
+      const int k0 = key0_t + j * C::kBN;  // first key of this K/V tile
       const int lim_lo = MASK == kMaskWindow ? min(C::kBN, max(0, row_key_lo - k0)) : 0;
       const int lim_hi = min(C::kBN, max(0, row_key_end - k0));
       const bool masked = lim_lo > 0 || lim_hi < C::kBN;
@@ -660,7 +665,7 @@ __global__ void __launch_bounds__(Cfg<D, TILES>::kThreads, Cfg<D, TILES>::kMinBl
             if (mbar_wait(bar(kBarEpi + t), 0, abort_flag)) {
               const uint32_t src = base + C::kQOff + static_cast<uint32_t>(t) * C::kTileBytes;
 #pragma unroll
-              for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(&tmO, src + b * C::kBoxBytes, b * 64, row0[t], bh);
+              for (int b = 0; b < C::kBoxes; ++b) tma_store_3d(&tmO, src + b * C::kBoxBytes, b * 64, row0_t, bh);
               bulk_commit_group();
               bulk_wait_group_read0();
             } else {
