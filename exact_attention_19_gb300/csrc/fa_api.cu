@@ -88,10 +88,9 @@ bool set_smem_attrs() {
             set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
-  if constexpr (D == 128)
-    ok = ok && launch_regs_are(fa::fa_fwd_persist_kernel<128>, fa::PCfg<128>::kRegLaunch) &&
-         cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(fa::PCfg<128>::kSmemBytes)) == cudaSuccess;
+  ok = ok && launch_regs_are(fa::fa_fwd_persist_kernel<D>, fa::PCfg<D>::kRegLaunch) &&
+       cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                            static_cast<int>(fa::PCfg<D>::kSmemBytes)) == cudaSuccess;
   if constexpr (D == 64)
     ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess &&
          set_smem_attr<64, fa::kMaskNone, true, 1>() == cudaSuccess &&
@@ -168,6 +167,9 @@ int launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, 
 // (8 x 12 x 1024: +5.5%, 2 x 4 x 2048: +8%; 4 x 32 x 8192: -10%, so longer
 // key ranges keep two tiles per CTA).
 constexpr int kSingleTileMaxKeys = 2048;
+// d = 64 without a mask: the persistent kernel up to this many keys (4 x 32 x
+// 8192: 1.6% slower than one CTA per unit; 8 x 12 x 1024: 9% faster).
+constexpr int kPersistD64MaxKeys = 2048;
 
 // no mask or the causal mask (split or not)
 template <int D, bool SPLIT>
@@ -275,29 +277,33 @@ void split_shape(int Nk, int n_splits, int* split_tiles, int* eff_splits) {
   *eff_splits = (n_kv + *split_tiles - 1) / *split_tiles;
 }
 
-// The persistent d = 128 kernel: one CTA per multiprocessor, at most one per
-// work unit (a head's pair of 128-row query tiles).
-int launch_persist128(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
-                      long long n_units, int sms, cudaStream_t stream) {
-  using C = fa::PCfg<128>;
+// The persistent kernel: one CTA per multiprocessor, at most one per work
+// unit (a head's pair of 128-row query tiles).
+template <int D>
+int launch_persist(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const fa::FwdParams& p,
+                   long long n_units, int sms, cudaStream_t stream) {
+  using C = fa::PCfg<D>;
   if (n_units >= (1ll << 31)) return FA_ERR_SHAPE;
   const long long grid = n_units < sms ? n_units : sms;
-  fa::fa_fwd_persist_kernel<128><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
+  fa::fa_fwd_persist_kernel<D><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
       mq, mk, mv, p, static_cast<int>(n_units));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 // Single-pass forward (no mask or causal) on prepared maps and parameters.
-// d = 128 without a mask: the persistent kernel (units of equal length,
-// balanced by its static schedule).  Causal: one CTA per unit, so the
-// hardware's dispatch balances units of unequal length in their longest-first
-// launch order; d = 64: one CTA per unit as well (measured as fast).
+// Without a mask, at d = 128 or at d = 64 with at most kPersistD64MaxKeys
+// keys: the persistent kernel (units of equal length, balanced by its static
+// schedule; at d = 64 it pays only on short units).  Causal: one CTA per
+// unit, so the hardware's dispatch balances units of unequal length in their
+// longest-first launch order.
 int launch_single_pass(int B, int H, int Nq, int Nk, int d, int causal, const CUtensorMap& mq,
                        const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, fa::FwdParams p,
                        int dev, cudaStream_t stream) {
-  if (d == 128 && !causal)
-    return launch_persist128(mq, mk, mv, p, static_cast<long long>(B) * H * p.n_pairs, g_dev_sms_or(dev, 148),
-                             stream);
+  if (!causal && (d == 128 || Nk <= kPersistD64MaxKeys)) {
+    const long long n_units = static_cast<long long>(B) * H * p.n_pairs;
+    return d == 64 ? launch_persist<64>(mq, mk, mv, p, n_units, g_dev_sms_or(dev, 148), stream)
+                   : launch_persist<128>(mq, mk, mv, p, n_units, g_dev_sms_or(dev, 148), stream);
+  }
   if (d == 64 && causal && Nk <= kSingleTileMaxKeys) {
     p.n_pairs = (Nq + 127) / 128;  // one query tile per CTA
     const long long grid = static_cast<long long>(B) * H * p.n_pairs;

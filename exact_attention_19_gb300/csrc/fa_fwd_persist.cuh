@@ -1,5 +1,5 @@
 // fa_fwd_persist.cuh -- persistent fused exact-attention forward for sm_103a
-// (d = 128, no mask, no K/V split).
+// (no mask, no K/V split; d = 128, and d = 64 for short key ranges).
 //
 // The arithmetic is that of fa_fwd_kernel (FA2 loop order, page "llm-infra-
 // atlas / FlashAttention 01", sections 2-4; conditional rescaling with
@@ -15,7 +15,8 @@
 //    the tensor pipe sees no start or end of a unit, and no CTA is launched,
 //    set up or torn down per unit.
 //  * 12 warps, launched with 168 registers each; setmaxnreg then gives
-//    warps 0-7 184 and warps 8-11 128 (as in fa_fwd_kernel):
+//    warps 0-7 184 and warps 8-11 128, or 192 and 120 at d = 64 (as in
+//    fa_fwd_kernel):
 //      warps 0-3   softmax, conditional rescale and epilogue of query tile 0
 //      warps 4-7   the same for query tile 1
 //      warp  8     TMA producer of the K/V ring
@@ -29,14 +30,13 @@
 //    thread; LSE) runs in that tile's softmax warps before they take the next
 //    unit's first S, so the next unit's first P V (which overwrites O) cannot
 //    start before O has been read.
-//  * One Q buffer per tile; the next unit's Q is loaded as soon as the last S
-//    product of the unit has read the old one (it was prefetched into L2 a
-//    unit earlier).  The Q-buffer bookkeeping below is written for kQBufs
-//    buffers per tile; at d = 128 shared memory holds one.
-//  * Only d = 128 without a mask is built: at d = 64 this schedule measured
-//    no faster than fa_fwd_kernel's one-CTA-per-unit launch, and causal units
-//    of unequal length are balanced better by the hardware's dispatch of
-//    fa_fwd_kernel's longest-first grid than by a static schedule.
+//  * d = 128: one Q buffer per tile; the next unit's Q is loaded as soon as
+//    the last S product of the unit has read the old one (it was prefetched
+//    into L2 a unit earlier).  d = 64: two Q buffers per tile, so the next
+//    unit's Q is loaded while the unit runs.
+//  * Causal units of unequal length are balanced better by the hardware's
+//    dispatch of fa_fwd_kernel's longest-first grid than by a static
+//    schedule, so only the no-mask case is built.
 #pragma once
 
 #include <cstdint>
@@ -48,12 +48,12 @@ namespace fa {
 
 template <int D>
 struct PCfg {
-  static_assert(D == 128, "the persistent schedule is built for d = 128 only");
+  static_assert(D == 64 || D == 128, "head dim");
   static constexpr int kThreads = 384;  // three warpgroups
   static constexpr int kWarpKV = 8, kWarpMma = 9, kWarpQ = 10;
   static constexpr int kBM = 128, kBN = 128;
-  static constexpr int kQBufs = 1;  // Q buffers per query tile
-  static constexpr int kRing = 5;   // K/V ring slots
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;  // Q buffers per query tile
+  static constexpr int kRing = (D == 64) ? 8 : 5;    // K/V ring slots
   static constexpr int kBoxes = D / 64;
   static constexpr uint32_t kBoxBytes = 128u * 128u;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
@@ -67,7 +67,7 @@ struct PCfg {
   static constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
   static constexpr uint32_t kIdescO = idesc_bf16(128, D, true);
   // registers per thread: at launch (checked by the host), softmax warpgroups, warpgroup 2
-  static constexpr int kRegLaunch = 168, kRegSoftmax = 184, kRegMisc = 128;
+  static constexpr int kRegLaunch = 168, kRegSoftmax = (D == 64) ? 192 : 184, kRegMisc = (D == 64) ? 120 : 128;
   static_assert(2 * 128 * kRegSoftmax + 128 * kRegMisc <= kThreads * kRegLaunch, "register split");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };

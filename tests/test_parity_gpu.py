@@ -149,18 +149,21 @@ def test_many_short_heads(d, causal):
     _check_full(synth.Workload("many", 16, 128, 130, 130, d, causal, seed=40 + d + causal), 1)
 
 
-# the persistent d = 128 kernel (a single pass without a mask): more work units
+# the persistent kernel (a single pass without a mask): more work units
 # than multiprocessors, so each CTA streams several units through one K/V ring
 # and one MMA stream; units whose second query tile is absent (Nq = 300: the
 # second pair holds one tile) or two rows long, key counts that are not tile
 # multiples, one key tile (S of the next unit issued in a unit's first step),
 # and fewer units than multiprocessors
+# (d = 64 takes the persistent kernel for up to 2048 keys: its two Q buffers
+# per tile rotate across units)
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("shape", [(2, 80, 300, 1000), (1, 160, 256, 640), (3, 53, 130, 2000), (4, 40, 129, 100),
                                    (1, 3, 1000, 4097)])
-def test_persistent_unit_stream(shape):
+def test_persistent_unit_stream(shape, d):
     B, H, nq, nk = shape
-    _check_full(synth.Workload("persist", B, H, nq, nk, 128, False, seed=50 + H), 1)
-    _check_full(synth.Workload("persist_wide", B, H, nq, nk, 128, False, sigma_q=8.0, seed=60 + H))
+    _check_full(synth.Workload("persist", B, H, nq, nk, d, False, seed=50 + H + d), 1)
+    _check_full(synth.Workload("persist_wide", B, H, nq, nk, d, False, sigma_q=8.0, seed=60 + H + d))
 
 
 # --- degenerate and numerically hard cases -----------------------------------
@@ -241,7 +244,7 @@ def test_deterministic():
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
-@pytest.mark.parametrize("mode", ["causal_d128", "full_d128", "full_d128_o16", "causal_d64_single_tile", "full_d64",
+@pytest.mark.parametrize("mode", ["causal_d128", "full_d128", "full_d128_o16", "causal_d64_single_tile", "full_d64", "full_d64_o16",
                                   "window_d128", "split_d64", "split_causal_d128"])
 def test_outputs_not_written_outside(mode):
     """O and LSE embedded in larger guard-filled buffers: the guards stay untouched.
