@@ -58,11 +58,14 @@ def kernel_source_hash() -> str:
 
 def kernel_name(w, n_splits) -> str:
     """The forward kernel the library launches for this workload: the persistent one for a single
-    pass without a mask (fa_fwd and fa_fwd_splitkv with one split) at d = 128, or at d = 64 with at
-    most 2048 keys; else fa_fwd_kernel."""
+    pass (fa_fwd and fa_fwd_splitkv with one split) without a mask at d = 128 or at d = 64 with at
+    most 2048 keys, and causal at d = 64 with more than 2048 keys; else fa_fwd_kernel."""
     single = n_splits is None or n_splits <= 1
-    if single and not w.causal and w.window is None and (w.d == 128 or w.Nk <= 2048):
-        return "fa_fwd_persist_kernel"
+    if single and w.window is None:
+        if not w.causal and (w.d == 128 or w.Nk <= 2048):
+            return "fa_fwd_persist_kernel"
+        if w.causal and w.d == 64 and w.Nk > 2048:
+            return "fa_fwd_persist_kernel"
     return "fa_fwd_kernel"
 
 

@@ -67,6 +67,13 @@ cudaError_t set_smem_attr() {
 }
 
 template <int D, int MASK>
+bool set_persist_attr() {
+  return launch_regs_are(fa::fa_fwd_persist_kernel<D, MASK>, fa::PCfg<D>::kRegLaunch) &&
+         cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(fa::PCfg<D>::kSmemBytes)) == cudaSuccess;
+}
+
+template <int D, int MASK>
 bool set_bwd_smem_attr() {
   using C = fa::BwdCfg<D>;
   return cudaFuncSetAttribute(fa::fa_bwd_dq_kernel<D, MASK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -88,9 +95,8 @@ bool set_smem_attrs() {
             set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
-  ok = ok && launch_regs_are(fa::fa_fwd_persist_kernel<D>, fa::PCfg<D>::kRegLaunch) &&
-       cudaFuncSetAttribute(fa::fa_fwd_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                            static_cast<int>(fa::PCfg<D>::kSmemBytes)) == cudaSuccess;
+  ok = ok && set_persist_attr<D, fa::kMaskNone>();
+  if constexpr (D == 64) ok = ok && set_persist_attr<64, fa::kMaskCausal>();
   if constexpr (D == 64)
     ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess &&
          set_smem_attr<64, fa::kMaskNone, true, 1>() == cudaSuccess &&
@@ -285,17 +291,33 @@ int launch_persist(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
   using C = fa::PCfg<D>;
   if (n_units >= (1ll << 31)) return FA_ERR_SHAPE;
   const long long grid = n_units < sms ? n_units : sms;
-  fa::fa_fwd_persist_kernel<D><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
+  fa::fa_fwd_persist_kernel<D, fa::kMaskNone><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes, stream>>>(
       mq, mk, mv, p, static_cast<int>(n_units));
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+// The causal persistent kernel (d = 64): one CTA per unit in the causal launch
+// order; running CTAs take over the ones not yet started (cluster launch
+// control).
+int launch_persist_causal64(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                            const fa::FwdParams& p, long long n_units, cudaStream_t stream) {
+  using C = fa::PCfg<64>;
+  if (n_units >= (1ll << 31)) return FA_ERR_SHAPE;
+  fa::fa_fwd_persist_kernel<64, fa::kMaskCausal>
+      <<<static_cast<unsigned>(n_units), C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p, static_cast<int>(n_units));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
 // Single-pass forward (no mask or causal) on prepared maps and parameters.
 // Without a mask, at d = 128 or at d = 64 with at most kPersistD64MaxKeys
 // keys: the persistent kernel (units of equal length, balanced by its static
-// schedule; at d = 64 it pays only on short units).  Causal: one CTA per
-// unit, so the hardware's dispatch balances units of unequal length in their
-// longest-first launch order.
+// schedule; at d = 64 it pays only on short units).  Causal at d = 64: single
+// query tiles, two CTAs per SM, up to kSingleTileMaxKeys keys; beyond, the
+// persistent kernel under cluster launch control (4 x 32 x 8192: +5%).
+// Causal at d = 128: one CTA per unit, so the hardware's dispatch balances
+// units of unequal length in their longest-first launch order (the dynamic
+// persistent schedule measured level on 4 x 32 x 8192 and 1.4-4.6% slower on
+// 1 x 16 x 32000).
 int launch_single_pass(int B, int H, int Nq, int Nk, int d, int causal, const CUtensorMap& mq,
                        const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, fa::FwdParams p,
                        int dev, cudaStream_t stream) {
@@ -310,6 +332,8 @@ int launch_single_pass(int B, int H, int Nq, int Nk, int d, int causal, const CU
     if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
     return launch<64, fa::kMaskCausal, false, 1>(mq, mk, mv, mo, p, grid, stream);
   }
+  if (d == 64 && causal)
+    return launch_persist_causal64(mq, mk, mv, p, static_cast<long long>(B) * H * p.n_pairs, stream);
   const long long grid = static_cast<long long>(B) * H * p.n_pairs;
   return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, mo, p, grid, stream)
                  : launch_d<128, false>(causal, mq, mk, mv, mo, p, grid, stream);

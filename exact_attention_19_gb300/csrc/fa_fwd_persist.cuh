@@ -1,5 +1,7 @@
 // fa_fwd_persist.cuh -- persistent fused exact-attention forward for sm_103a
-// (no mask, no K/V split; d = 128, and d = 64 for short key ranges).
+// (no K/V split).  Without a mask: d = 128, and d = 64 for short key ranges,
+// under a static schedule.  Causal at d = 64 for long key ranges: under a
+// dynamic schedule (cluster launch control).
 //
 // The arithmetic is that of fa_fwd_kernel (FA2 loop order, page "llm-infra-
 // atlas / FlashAttention 01", sections 2-4; conditional rescaling with
@@ -34,9 +36,13 @@
 //    the last S product of the unit has read the old one (it was prefetched
 //    into L2 a unit earlier).  d = 64: two Q buffers per tile, so the next
 //    unit's Q is loaded while the unit runs.
-//  * Causal units of unequal length are balanced better by the hardware's
-//    dispatch of fa_fwd_kernel's longest-first grid than by a static
-//    schedule, so only the no-mask case is built.
+//  * Causal units are of unequal length (1 to N / 128 K/V tiles): the grid
+//    keeps one CTA per unit in fa_fwd_kernel's longest-first order, and a
+//    running CTA asks the hardware for the next CTA not yet started
+//    (clusterlaunchcontrol.try_cancel) and runs its unit instead, so the
+//    hardware's greedy balance of that order is kept.  The K/V producer asks
+//    for unit k + 1 as it starts unit k; the answers pass to the other roles
+//    through a ring of kUnitRing 16-byte slots in shared memory.
 #pragma once
 
 #include <cstdint>
@@ -54,6 +60,7 @@ struct PCfg {
   static constexpr int kBM = 128, kBN = 128;
   static constexpr int kQBufs = (D == 64) ? 2 : 1;  // Q buffers per query tile
   static constexpr int kRing = (D == 64) ? 8 : 5;    // K/V ring slots
+  static constexpr int kUnitRing = 4;                // dynamic schedule: unit responses in flight
   static constexpr int kBoxes = D / 64;
   static constexpr uint32_t kBoxBytes = 128u * 128u;
   static constexpr uint32_t kTileBytes = kBoxes * kBoxBytes;
@@ -80,9 +87,15 @@ enum : int {
   kPBarP = 10,       // [t]
   kPBarOFinal = 12,  // [t]
   kPBarDrain = 14,
-  kPBarRing = 15     // full[kRing] then empty[kRing]
+  kPBarRing = 15,      // full[kRing] then empty[kRing] (kRing <= 8)
+  kPBarUnit = 31,      // dynamic schedule: response s has landed [kUnitRing]
+  kPBarUnitFree = 35,  // dynamic schedule: every consumer has read response s [kUnitRing]
+  kPBarEnd = 39
 };
-static_assert(8 * (kPBarRing + 16) <= 448, "barrier block");
+constexpr uint32_t kUnitRespOff = 320;  // kUnitRing 16-byte responses, after the barriers
+static_assert(8 * kPBarEnd <= kUnitRespOff && kUnitRespOff + 16 * 4 <= 448, "barrier block");
+// consumers of a unit response: the Q producer, the MMA warp, the 8 softmax warps
+constexpr int kUnitConsumers = 10;
 
 // L2 prefetch of one TMA box (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x, int y, int z) {
@@ -100,10 +113,16 @@ struct PUnit {
   int n_max;       // K/V tiles streamed: max(jhi)
 };
 
-template <int D>
+// MASK kMaskNone: a static schedule over min(units, SMs) CTAs.  kMaskCausal:
+// one CTA per unit in fa_fwd_kernel's causal launch order; a running CTA
+// takes over CTAs that have not started yet with cluster launch control, so
+// the hardware's greedy dispatch of that order is kept.
+template <int D, int MASK>
 __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     fa_fwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const FwdParams p, const int n_units) {
+  static_assert(MASK == kMaskNone || MASK == kMaskCausal, "no mask or causal");
+  constexpr bool kDynamic = MASK == kMaskCausal;
   using C = PCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_addr(smem_raw);
@@ -137,6 +156,10 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
+    for (int s = 0; s < C::kUnitRing; ++s) {
+      mbar_init(bar(kPBarUnit + s), 1);
+      mbar_init(bar(kPBarUnitFree + s), kUnitConsumers);
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -153,22 +176,72 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
   const int G = static_cast<int>(gridDim.x);
   const int cta = static_cast<int>(blockIdx.x);
   const int n_kv = (p.Nk + C::kBN - 1) / C::kBN;
-  // k-th unit of this CTA, or false past the end
-  auto unit_at = [&](int k, PUnit& u) -> bool {
-    const long long id = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - cta) : cta);
-    if (id >= n_units) return false;
-    const int uid = static_cast<int>(id);
-    const int pair = uid % p.n_pairs;
-    u.bh = uid / p.n_pairs;
+  // the unit with index uid in launch order
+  auto decode = [&](int uid, PUnit& u) {
+    int bh = uid / p.n_pairs, pair = uid % p.n_pairs;
+    if (MASK == kMaskCausal) {
+      // heads in groups whose K/V fit a quarter of the L2, heaviest pairs of
+      // a group first (fa_fwd_kernel's causal launch order)
+      const int n_bh = n_units / p.n_pairs;
+      const int per_group = p.lpt_group * p.n_pairs;
+      const int grp = uid / per_group;
+      const int g0 = grp * p.lpt_group;
+      const int g_heads = min(p.lpt_group, n_bh - g0);
+      const int within = uid - grp * per_group;
+      bh = g0 + within % g_heads;
+      pair = p.n_pairs - 1 - within / g_heads;
+    }
+    u.bh = bh;
     u.n_max = 0;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int qt = 2 * pair + t;
       u.row0[t] = qt * C::kBM;
       u.jhi[t] = 0;
-      if (u.row0[t] < p.Nq) u.jhi[t] = n_kv;
+      if (u.row0[t] < p.Nq) u.jhi[t] = (MASK == kMaskCausal) ? min(n_kv, qt + 1) : n_kv;
       u.n_max = max(u.n_max, u.jhi[t]);
     }
+  };
+  // Dynamic schedule: unit k >= 1 of this CTA is the answer to the k-th
+  // cancellation request, in response slot (k - 1) % kUnitRing.
+  auto resp_addr = [&](int s) -> uint32_t { return bar0 + kUnitRespOff + 16u * static_cast<uint32_t>(s); };
+  // The k-th unit of this CTA: 1 with u filled in, 0 past the end, -1 when a
+  // wait gave up.  `release`: 0 for the requesting thread, 1 for a single
+  // consuming thread, 2 for a whole consuming warp (lane 0 releases the slot).
+  auto get_unit = [&](int k, PUnit& u, int release) -> int {
+    if constexpr (!kDynamic) {
+      const long long id = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - cta) : cta);
+      if (id >= n_units) return 0;
+      decode(static_cast<int>(id), u);
+      return 1;
+    } else {
+      if (k == 0) {
+        decode(cta, u);
+        return 1;
+      }
+      const int s = (k - 1) % C::kUnitRing;
+      bool got = mbar_wait(bar(kPBarUnit + s), ((k - 1) / C::kUnitRing) & 1, abort_flag);
+      if (release == 2) got = __all_sync(0xffffffffu, got);
+      if (!got) return -1;
+      int x = 0;
+      const bool more = clc_query(resp_addr(s), x);
+      if (release == 2) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kPBarUnitFree + s));
+      } else if (release == 1) {
+        mbar_arrive(bar(kPBarUnitFree + s));
+      }
+      if (!more) return 0;
+      decode(x, u);
+      return 1;
+    }
+  };
+  // Dynamic schedule, requesting thread only: ask for the CTA's unit k.
+  auto request_unit = [&](int k) -> bool {
+    const int s = (k - 1) % C::kUnitRing, use = (k - 1) / C::kUnitRing;
+    if (use > 0 && !mbar_wait(bar(kPBarUnitFree + s), (use - 1) & 1, abort_flag)) return false;
+    mbar_arrive_expect_tx(bar(kPBarUnit + s), 16);
+    clc_try_cancel(resp_addr(s), bar(kPBarUnit + s));
     return true;
   };
 
@@ -180,8 +253,20 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       tma_prefetch_map(&tmV);
       int issued = 0;
       bool ok = true;
+      int pending = 0;  // dynamic: unit whose request is answered but not yet read (0: none)
       PUnit u;
-      for (int k = 0; ok && unit_at(k, u); ++k) {
+      int r = get_unit(0, u, 0);
+      for (int k = 0; ok && r == 1; ++k) {
+        // dynamic: ask now for the next unit; its answer is needed once this
+        // unit's loads have been issued
+        if (kDynamic) {
+          if (!request_unit(k + 1)) {
+            report_wait_failure(abort_flag, 2u);
+            ok = false;
+            break;
+          }
+          pending = k + 1;
+        }
         for (int i = 0; i < 2 * u.n_max; ++i) {
           const int item = issued;
           const int s = item % C::kRing;
@@ -196,11 +281,22 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
             tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (i >> 1) * C::kBN, u.bh);
           issued = item + 1;
         }
+        if (!ok) break;
+        r = get_unit(k + 1, u, 0);
+        if (r < 0) {
+          report_wait_failure(abort_flag, 2u);
+          ok = false;
+        } else {
+          pending = 0;
+        }
       }
       if (*abort_flag) {
         // let every copy already issued land before the CTA can exit
         for (int item = max(0, issued - C::kRing); item < issued; ++item)
           mbar_wait(full(item % C::kRing), (item / C::kRing) & 1, nullptr);
+        // and the answer to an outstanding cancellation request
+        if (kDynamic && pending > 0)
+          mbar_wait(bar(kPBarUnit + (pending - 1) % C::kUnitRing), ((pending - 1) / C::kUnitRing) & 1, nullptr);
       }
     } else if (warp == C::kWarpQ && lane == 0) {
       // ======================= Q producer =================================
@@ -208,7 +304,8 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
       int occ[2] = {0, 0};
       bool ok = true;
       PUnit u, un;
-      for (int k = 0; ok && unit_at(k, u); ++k) {
+      int r = get_unit(0, u, 1);
+      for (int k = 0; ok && r == 1; ++k) {
         for (int t = 0; t < 2 && ok; ++t) {
           if (u.jhi[t] == 0) continue;
           const int qb = occ[t] % C::kQBufs, use = occ[t] / C::kQBufs;
@@ -223,11 +320,17 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
                         u.bh);
           ++occ[t];
         }
+        if (!ok) break;
         // the next unit's Q into L2 while this one runs
-        if (ok && unit_at(k + 1, un)) {
+        r = get_unit(k + 1, un, 1);
+        if (r < 0) {
+          report_wait_failure(abort_flag, 2u);
+          ok = false;
+        } else if (r == 1) {
           for (int t = 0; t < 2; ++t)
             if (un.jhi[t] > 0)
               for (int b = 0; b < C::kBoxes; ++b) tma_prefetch_l2_3d(&tmQ, b * 64, un.row0[t], un.bh);
+          u = un;
         }
       }
       if (*abort_flag) {
@@ -397,7 +500,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         if (has_k) mma_commit_elect(empty(sk));
         return true;
       };
-      if (unit_at(0, cur)) {
+      if (get_unit(0, cur, 2) == 1) {
         // prologue: the first unit's first S products
         for (int t = 0; t < 2 && ok; ++t)
           if (cur.jhi[t] > 0) ok = uniform(mbar_wait(bar(kPBarQFull + t), 0, abort_flag));
@@ -413,7 +516,12 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
           mma_commit_elect(empty(0));
         }
         for (int k = 0; ok; ++k) {
-          has_nxt = unit_at(k + 1, nxt);
+          const int rn = get_unit(k + 1, nxt, 2);
+          if (rn < 0) {
+            ok = false;
+            break;
+          }
+          has_nxt = rn == 1;
           for (int t = 0; t < 2; ++t) {
             occ_n[t] = occ[t] + (cur.jhi[t] > 0 ? 1 : 0);
             qb[t] = occ[t] % C::kQBufs;
@@ -458,11 +566,18 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     int occ = 0;  // units in which this tile was present so far (O-final phases)
     bool ok = true;
     PUnit u;
-    for (int k = 0; ok && unit_at(k, u); ++k) {
+    for (int k = 0; ok; ++k) {
+      const int r = get_unit(k, u, 2);
+      if (r < 0) {
+        ok = false;
+        break;
+      }
+      if (r == 0) break;
       const int nt = u.jhi[t];
       if (nt == 0) continue;
       const int row = u.row0[t] + row_local;
-      const int row_key_end = p.Nk;  // keys past Nk (the ragged last tile) are masked
+      // keys past Nk (the ragged last tile) and, causal, past the row are masked
+      const int row_key_end = (MASK == kMaskCausal) ? min(p.Nk, row + 1) : p.Nk;
       float m_bar = NEG_INF;  // reference maximum, base-2 scaled units
       float l = 0.f;
       float r_max = NEG_INF;  // the row's largest score (raw units); see fa_fwd_kernel

@@ -129,6 +129,34 @@ __device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t (&r)[8]) 
                : "memory");
 }
 
+// Cluster launch control.  clc_try_cancel asks the hardware to cancel a CTA
+// of this grid that has not started yet (the next one in launch order); the
+// 16-byte response lands at `resp` and completes 16 bytes of transaction on
+// `bar`.  A grid must issue no further request after one has failed.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile("fence.proxy.async.shared::cta;\n\t"
+               "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                   resp),
+               "r"(bar)
+               : "memory");
+}
+// Decodes a response: true with the cancelled CTA's x index, or false when no
+// CTA was left to cancel.
+__device__ __forceinline__ bool clc_query(uint32_t resp, int& ctaid_x) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b128 h;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(resp)
+      : "memory");
+  ctaid_x = static_cast<int>(x);
+  return ok != 0;
+}
+
 // Tiled TMA store shared -> global, completion tracked by bulk groups.  x must
 // be a multiple of 8 for bf16 and no coordinate may be negative; elements of
 // the box outside the tensor are not written.

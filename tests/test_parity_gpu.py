@@ -166,6 +166,28 @@ def test_persistent_unit_stream(shape, d):
     _check_full(synth.Workload("persist_wide", B, H, nq, nk, d, False, sigma_q=8.0, seed=60 + H + d))
 
 
+# causal d = 64 beyond 2048 keys: the persistent kernel under cluster launch
+# control (a running CTA takes over the units of CTAs not yet started; units of
+# 1 to N / 128 K/V tiles, a ragged last tile, more units than multiprocessors)
+@pytest.mark.parametrize("shape", [(2, 40, 2304), (1, 20, 3000), (3, 7, 2049)])
+def test_causal_d64_dynamic_schedule(shape):
+    B, H, n = shape
+    _check_full(synth.Workload("clc", B, H, n, n, 64, True, seed=70 + H), 1)
+    _check_full(synth.Workload("clc_wide", B, H, n, n, 64, True, sigma_q=8.0, seed=80 + H), 1)
+
+
+def test_causal_d64_dynamic_schedule_full_size():
+    w = synth.WORKLOADS["long_8192_d64"].with_(name="long_8192_d64_causal", causal=True)
+    q, k, v = w.make()
+    o, lse = run_gpu(q, k, v, w.scale, True)
+    rows = sample_rows(w.B, w.H, w.Nq, 300, seed=w.seed)
+    o_ref, lse_ref = oracle.attention_rows(q, k, v, rows, w.scale, True)
+    assert_close(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.name)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    # row 0 of every head sees key 0 only: O = V[0] exactly
+    assert np.array_equal(o[:, :, 0, :], synth.bf16_to_f32(v[:, :, 0, :]).astype(np.float64))
+
+
 # --- degenerate and numerically hard cases -----------------------------------
 @pytest.mark.parametrize("d", [64, 128])
 def test_single_key(d):
