@@ -663,6 +663,8 @@ def main(argv=None):
     ap.add_argument("--window", default=None, metavar="LEFT,RIGHT",
                     help="sliding-window mask over the workload (bottom-right, -1 = open side); "
                          "FLOPs then count 4*d per kept (row, key) pair")
+    ap.add_argument("--causal", action="store_true",
+                    help="apply the causal mask to the workload (square workloads only; FLOPs halved)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -677,6 +679,13 @@ def main(argv=None):
         if wl < -1 or wr < -1:
             ap.error("--window bounds must be >= -1")
         w = w.with_(window=(wl, wr), causal=False)
+    if args.causal:
+        if args.window is not None:
+            ap.error("--causal and --window exclude each other")
+        if w.Nq != w.Nk:
+            ap.error("--causal needs a square workload (Nq == Nk)")
+        if not w.causal:
+            w = w.with_(causal=True, name=w.name + "_causal")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

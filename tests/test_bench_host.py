@@ -64,6 +64,11 @@ def test_kernel_name_follows_dispatch():
     assert bench.kernel_name(w.with_(window=(64, 0)), None) == "fa_fwd_kernel"
 
 
+def test_causal_flag_rejects_window():
+    with pytest.raises(SystemExit):
+        bench.main(["--causal", "--window", "64,0"])
+
+
 def test_traffic_lookup(tmp_path, monkeypatch):
     h = bench.kernel_source_hash()
     f = tmp_path / "traffic.md"
