@@ -176,6 +176,11 @@ constexpr int kSingleTileMaxKeys = 2048;
 // d = 64 without a mask: the persistent kernel up to this many keys (4 x 32 x
 // 8192: 1.6% slower than one CTA per unit; 8 x 12 x 1024: 9% faster).
 constexpr int kPersistD64MaxKeys = 2048;
+// Causal d = 64 beyond kSingleTileMaxKeys keys: the persistent kernel under
+// cluster launch control once there are this many query-tile pairs per SM
+// (fewer, and single tiles balance better: causal 4 x 16 x 3072, 5 pairs per
+// SM, 6% faster on single tiles; 4 x 16 x 4096, 6.7 per SM, 2.5% slower).
+constexpr int kClcMinUnitsPerSm = 6;
 
 // no mask or the causal mask (split or not)
 template <int D, bool SPLIT>
@@ -312,8 +317,9 @@ int launch_persist_causal64(const CUtensorMap& mq, const CUtensorMap& mk, const 
 // Without a mask, at d = 128 or at d = 64 with at most kPersistD64MaxKeys
 // keys: the persistent kernel (units of equal length, balanced by its static
 // schedule; at d = 64 it pays only on short units).  Causal at d = 64: single
-// query tiles, two CTAs per SM, up to kSingleTileMaxKeys keys; beyond, the
-// persistent kernel under cluster launch control (4 x 32 x 8192: +5%).
+// query tiles, two CTAs per SM, up to kSingleTileMaxKeys keys or below
+// kClcMinUnitsPerSm pairs per SM; beyond, the persistent kernel under cluster
+// launch control (4 x 32 x 8192: +5%).
 // Causal at d = 128: one CTA per unit, so the hardware's dispatch balances
 // units of unequal length in their longest-first launch order (the dynamic
 // persistent schedule measured level on 4 x 32 x 8192 and 1.4-4.6% slower on
@@ -321,19 +327,19 @@ int launch_persist_causal64(const CUtensorMap& mq, const CUtensorMap& mk, const 
 int launch_single_pass(int B, int H, int Nq, int Nk, int d, int causal, const CUtensorMap& mq,
                        const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, fa::FwdParams p,
                        int dev, cudaStream_t stream) {
+  const long long n_units = static_cast<long long>(B) * H * p.n_pairs;  // query-tile pairs
   if (!causal && (d == 128 || Nk <= kPersistD64MaxKeys)) {
-    const long long n_units = static_cast<long long>(B) * H * p.n_pairs;
     return d == 64 ? launch_persist<64>(mq, mk, mv, p, n_units, g_dev_sms_or(dev, 148), stream)
                    : launch_persist<128>(mq, mk, mv, p, n_units, g_dev_sms_or(dev, 148), stream);
   }
-  if (d == 64 && causal && Nk <= kSingleTileMaxKeys) {
+  if (d == 64 && causal &&
+      (Nk <= kSingleTileMaxKeys || n_units < kClcMinUnitsPerSm * static_cast<long long>(g_dev_sms_or(dev, 148)))) {
     p.n_pairs = (Nq + 127) / 128;  // one query tile per CTA
     const long long grid = static_cast<long long>(B) * H * p.n_pairs;
     if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
     return launch<64, fa::kMaskCausal, false, 1>(mq, mk, mv, mo, p, grid, stream);
   }
-  if (d == 64 && causal)
-    return launch_persist_causal64(mq, mk, mv, p, static_cast<long long>(B) * H * p.n_pairs, stream);
+  if (d == 64 && causal) return launch_persist_causal64(mq, mk, mv, p, n_units, stream);
   const long long grid = static_cast<long long>(B) * H * p.n_pairs;
   return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, mo, p, grid, stream)
                  : launch_d<128, false>(causal, mq, mk, mv, mo, p, grid, stream);

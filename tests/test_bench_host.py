@@ -61,6 +61,8 @@ def test_kernel_name_follows_dispatch():
     assert bench.kernel_name(synth.WORKLOADS["single_head_256_d64"], 1) == "fa_fwd_persist_kernel"
     assert bench.kernel_name(synth.WORKLOADS["gpt2_small_causal_1024_d64"], None) == "fa_fwd_kernel"
     assert bench.kernel_name(synth.WORKLOADS["long_8192_d64"].with_(causal=True), None) == "fa_fwd_persist_kernel"
+    few = synth.WORKLOADS["long_8192_d64"].with_(causal=True, B=1, H=8)  # 256 pairs: under 6 per SM
+    assert bench.kernel_name(few, None) == "fa_fwd_kernel"
     assert bench.kernel_name(w.with_(window=(64, 0)), None) == "fa_fwd_kernel"
 
 

@@ -22,7 +22,7 @@ def _rand(shape, gen):
     (1, 1, 4096, 64, False, True),    # split-KV: sliced forward + merge (programmatic dependent launch)
     (2, 40, 1000, 128, False, False),  # persistent kernel, static schedule, more units than SMs
     (4, 12, 512, 64, False, False),    # persistent kernel at d = 64 (two Q buffers per tile)
-    (2, 20, 2304, 64, True, False),    # persistent kernel under cluster launch control
+    (4, 64, 2200, 64, True, False),    # persistent kernel under cluster launch control
 ])
 def test_forward_graph_replay_matches_direct_calls(B, H, N, d, causal, split):
     gen = torch.Generator(device="cuda")

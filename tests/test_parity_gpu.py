@@ -166,10 +166,11 @@ def test_persistent_unit_stream(shape, d):
     _check_full(synth.Workload("persist_wide", B, H, nq, nk, d, False, sigma_q=8.0, seed=60 + H + d))
 
 
-# causal d = 64 beyond 2048 keys: the persistent kernel under cluster launch
-# control (a running CTA takes over the units of CTAs not yet started; units of
-# 1 to N / 128 K/V tiles, a ragged last tile, more units than multiprocessors)
-@pytest.mark.parametrize("shape", [(2, 40, 2304), (1, 20, 3000), (3, 7, 2049)])
+# causal d = 64 beyond 2048 keys: with at least 6 query-tile pairs per SM the
+# persistent kernel under cluster launch control (a running CTA takes over the
+# units of CTAs not yet started; units of 1 to N / 128 K/V tiles, a ragged last
+# tile); with fewer, single query tiles (the last two shapes)
+@pytest.mark.parametrize("shape", [(4, 64, 2200), (8, 16, 3000), (1, 20, 3000), (3, 7, 2049)])
 def test_causal_d64_dynamic_schedule(shape):
     B, H, n = shape
     _check_full(synth.Workload("clc", B, H, n, n, 64, True, seed=70 + H), 1)
