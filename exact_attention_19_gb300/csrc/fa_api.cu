@@ -95,8 +95,7 @@ bool set_smem_attrs() {
             set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
-  ok = ok && set_persist_attr<D, fa::kMaskNone>();
-  if constexpr (D == 64) ok = ok && set_persist_attr<64, fa::kMaskCausal>();
+  ok = ok && set_persist_attr<D, fa::kMaskNone>() && set_persist_attr<D, fa::kMaskCausal>();
   if constexpr (D == 64)
     ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess &&
          set_smem_attr<64, fa::kMaskNone, true, 1>() == cudaSuccess &&
@@ -181,6 +180,10 @@ constexpr int kPersistD64MaxKeys = 2048;
 // (fewer, and single tiles balance better: causal 4 x 16 x 3072, 5 pairs per
 // SM, 6% faster on single tiles; 4 x 16 x 4096, 6.7 per SM, 2.5% slower).
 constexpr int kClcMinUnitsPerSm = 6;
+// Causal d = 128: the same dynamic schedule from this many pairs per SM
+// (4 x 32 x 8192, 27 per SM: +1%; 1 x 16 x 32000, 13 per SM with units of up
+// to 250 K/V tiles: 4.6% slower, so one CTA per unit there).
+constexpr int kClcMinUnitsPerSm128 = 20;
 
 // no mask or the causal mask (split or not)
 template <int D, bool SPLIT>
@@ -301,14 +304,14 @@ int launch_persist(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
 
-// The causal persistent kernel (d = 64): one CTA per unit in the causal launch
-// order; running CTAs take over the ones not yet started (cluster launch
-// control).
-int launch_persist_causal64(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                            const fa::FwdParams& p, long long n_units, cudaStream_t stream) {
-  using C = fa::PCfg<64>;
+// The causal persistent kernel: one CTA per unit in the causal launch order;
+// running CTAs take over the ones not yet started (cluster launch control).
+template <int D>
+int launch_persist_causal(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                          const fa::FwdParams& p, long long n_units, cudaStream_t stream) {
+  using C = fa::PCfg<D>;
   if (n_units >= (1ll << 31)) return FA_ERR_SHAPE;
-  fa::fa_fwd_persist_kernel<64, fa::kMaskCausal>
+  fa::fa_fwd_persist_kernel<D, fa::kMaskCausal>
       <<<static_cast<unsigned>(n_units), C::kThreads, C::kSmemBytes, stream>>>(mq, mk, mv, p, static_cast<int>(n_units));
   return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
 }
@@ -320,10 +323,9 @@ int launch_persist_causal64(const CUtensorMap& mq, const CUtensorMap& mk, const 
 // query tiles, two CTAs per SM, up to kSingleTileMaxKeys keys or below
 // kClcMinUnitsPerSm pairs per SM; beyond, the persistent kernel under cluster
 // launch control (4 x 32 x 8192: +5%).
-// Causal at d = 128: one CTA per unit, so the hardware's dispatch balances
-// units of unequal length in their longest-first launch order (the dynamic
-// persistent schedule measured level on 4 x 32 x 8192 and 1.4-4.6% slower on
-// 1 x 16 x 32000).
+// Causal at d = 128: the dynamic persistent schedule from kClcMinUnitsPerSm128
+// pairs per SM; below, one CTA per unit, so the hardware's dispatch balances
+// long units of unequal length in their longest-first launch order.
 int launch_single_pass(int B, int H, int Nq, int Nk, int d, int causal, const CUtensorMap& mq,
                        const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, fa::FwdParams p,
                        int dev, cudaStream_t stream) {
@@ -339,7 +341,9 @@ int launch_single_pass(int B, int H, int Nq, int Nk, int d, int causal, const CU
     if (grid >= (1ll << 31)) return FA_ERR_SHAPE;
     return launch<64, fa::kMaskCausal, false, 1>(mq, mk, mv, mo, p, grid, stream);
   }
-  if (d == 64 && causal) return launch_persist_causal64(mq, mk, mv, p, n_units, stream);
+  if (d == 64 && causal) return launch_persist_causal<64>(mq, mk, mv, p, n_units, stream);
+  if (causal && n_units >= kClcMinUnitsPerSm128 * static_cast<long long>(g_dev_sms_or(dev, 148)))
+    return launch_persist_causal<128>(mq, mk, mv, p, n_units, stream);
   const long long grid = static_cast<long long>(B) * H * p.n_pairs;
   return d == 64 ? launch_d<64, false>(causal, mq, mk, mv, mo, p, grid, stream)
                  : launch_d<128, false>(causal, mq, mk, mv, mo, p, grid, stream);

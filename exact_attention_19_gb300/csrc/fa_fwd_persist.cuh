@@ -1,7 +1,7 @@
 // fa_fwd_persist.cuh -- persistent fused exact-attention forward for sm_103a
 // (no K/V split).  Without a mask: d = 128, and d = 64 for short key ranges,
-// under a static schedule.  Causal at d = 64 for long key ranges: under a
-// dynamic schedule (cluster launch control).
+// under a static schedule.  Causal with many query-tile pairs per SM (and at
+// d = 64 long key ranges): under a dynamic schedule (cluster launch control).
 //
 // The arithmetic is that of fa_fwd_kernel (FA2 loop order, page "llm-infra-
 // atlas / FlashAttention 01", sections 2-4; conditional rescaling with

@@ -56,7 +56,8 @@ def test_kernel_name_follows_dispatch():
     assert bench.kernel_name(w, None) == "fa_fwd_persist_kernel"
     assert bench.kernel_name(w, 1) == "fa_fwd_persist_kernel"
     assert bench.kernel_name(w, 4) == "fa_fwd_kernel"
-    assert bench.kernel_name(synth.WORKLOADS["long_8192_d128_causal"], None) == "fa_fwd_kernel"
+    assert bench.kernel_name(synth.WORKLOADS["long_8192_d128_causal"], None) == "fa_fwd_persist_kernel"
+    assert bench.kernel_name(synth.WORKLOADS["stress_32000_d128_causal"], None) == "fa_fwd_kernel"
     assert bench.kernel_name(synth.WORKLOADS["single_head_4096_d64"], 1) == "fa_fwd_kernel"
     assert bench.kernel_name(synth.WORKLOADS["single_head_256_d64"], 1) == "fa_fwd_persist_kernel"
     assert bench.kernel_name(synth.WORKLOADS["gpt2_small_causal_1024_d64"], None) == "fa_fwd_kernel"

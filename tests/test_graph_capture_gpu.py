@@ -23,6 +23,7 @@ def _rand(shape, gen):
     (2, 40, 1000, 128, False, False),  # persistent kernel, static schedule, more units than SMs
     (4, 12, 512, 64, False, False),    # persistent kernel at d = 64 (two Q buffers per tile)
     (4, 64, 2200, 64, True, False),    # persistent kernel under cluster launch control
+    (16, 48, 1100, 128, True, False),  # the same at d = 128 (20+ query-tile pairs per SM)
 ])
 def test_forward_graph_replay_matches_direct_calls(B, H, N, d, causal, split):
     gen = torch.Generator(device="cuda")

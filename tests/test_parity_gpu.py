@@ -177,6 +177,12 @@ def test_causal_d64_dynamic_schedule(shape):
     _check_full(synth.Workload("clc_wide", B, H, n, n, 64, True, sigma_q=8.0, seed=80 + H), 1)
 
 
+# causal d = 128 with at least 20 query-tile pairs per SM: the same dynamic
+# schedule (16 x 48 heads of 1100 rows: 3840 pairs, a ragged last tile)
+def test_causal_d128_dynamic_schedule():
+    _check_full(synth.Workload("clc128", 16, 48, 1100, 1100, 128, True, seed=91), 1)
+
+
 def test_causal_d64_dynamic_schedule_full_size():
     w = synth.WORKLOADS["long_8192_d64"].with_(name="long_8192_d64_causal", causal=True)
     q, k, v = w.make()
