@@ -60,9 +60,16 @@ def kernel_name(w, n_splits, sms: int = 152) -> str:
     """The forward kernel the library launches for this workload: the persistent one for a single
     pass (fa_fwd and fa_fwd_splitkv with one split) without a mask at d = 128 or at d = 64 with at
     most 2048 keys, causal at d = 64 with more than 2048 keys and at least 6 query-tile pairs per
-    SM, and causal at d = 128 with at least 20 pairs per SM; else fa_fwd_kernel."""
+    SM, causal at d = 128 with at least 20 pairs per SM, and a window bounded on both sides
+    with Nq <= Nk and at least 4 pairs per SM; else fa_fwd_kernel."""
     single = n_splits is None or n_splits <= 1
-    if single and w.window is None:
+    if w.window is not None:
+        wl, wr = w.window
+        pairs = w.B * w.H * ((w.Nq + 255) // 256)
+        if wl >= 0 and wr >= 0 and w.Nq <= w.Nk and pairs >= 4 * sms:
+            return "fa_fwd_persist_kernel"
+        return "fa_fwd_kernel"
+    if single:
         if not w.causal and (w.d == 128 or w.Nk <= 2048):
             return "fa_fwd_persist_kernel"
         pairs = w.B * w.H * ((w.Nq + 255) // 256)

@@ -95,7 +95,8 @@ bool set_smem_attrs() {
             set_smem_attr<D, fa::kMaskWindow, false>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskNone, true>() == cudaSuccess &&
             set_smem_attr<D, fa::kMaskCausal, true>() == cudaSuccess;
-  ok = ok && set_persist_attr<D, fa::kMaskNone>() && set_persist_attr<D, fa::kMaskCausal>();
+  ok = ok && set_persist_attr<D, fa::kMaskNone>() && set_persist_attr<D, fa::kMaskCausal>() &&
+       set_persist_attr<D, fa::kMaskWindow>();
   if constexpr (D == 64)
     ok = ok && set_smem_attr<64, fa::kMaskCausal, false, 1>() == cudaSuccess &&
          set_smem_attr<64, fa::kMaskNone, true, 1>() == cudaSuccess &&
@@ -184,6 +185,12 @@ constexpr int kClcMinUnitsPerSm = 6;
 // (4 x 32 x 8192, 27 per SM: +1%; 1 x 16 x 32000, 13 per SM with units of up
 // to 250 K/V tiles: 4.6% slower, so one CTA per unit there).
 constexpr int kClcMinUnitsPerSm128 = 20;
+// A window bounded on both sides with Nq <= Nk (every row sees a key, units
+// of about equal length): the persistent kernel's static schedule from this
+// many query-tile pairs per SM (4 x 32 x 8192 d = 64 band of 1024 keys: +6%;
+// 2 x 16 x 4096, 1.7 pairs per SM: 3% slower).  A band open on one side gives
+// units of unequal length, which the static schedule balances badly.
+constexpr int kPersistWindowMinUnitsPerSm = 4;
 
 // no mask or the causal mask (split or not)
 template <int D, bool SPLIT>
@@ -396,7 +403,19 @@ int fa_fwd_window(const void* q, const void* k, const void* v, void* o, float* l
   p.win_left = window_left;
   p.win_right = window_right;
   p.diag_off = Nk - Nq;  // bottom-right: the window's diagonal ends at (Nq - 1, Nk - 1)
-  const long long grid = static_cast<long long>(B) * H * p.n_pairs;
+  const long long grid = static_cast<long long>(B) * H * p.n_pairs;  // one CTA per query-tile pair
+  const int sms = g_dev_sms_or(dev, 148);
+  if (window_left >= 0 && window_right >= 0 && Nq <= Nk && grid < (1ll << 31) &&
+      grid >= kPersistWindowMinUnitsPerSm * static_cast<long long>(sms)) {
+    const unsigned pgrid = static_cast<unsigned>(grid < sms ? grid : sms);
+    if (d == 64)
+      fa::fa_fwd_persist_kernel<64, fa::kMaskWindow><<<pgrid, fa::PCfg<64>::kThreads, fa::PCfg<64>::kSmemBytes, stream>>>(
+          mq, mk, mv, p, static_cast<int>(grid));
+    else
+      fa::fa_fwd_persist_kernel<128, fa::kMaskWindow><<<pgrid, fa::PCfg<128>::kThreads, fa::PCfg<128>::kSmemBytes, stream>>>(
+          mq, mk, mv, p, static_cast<int>(grid));
+    return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  }
   if (window_left < 0 && window_right < 0)  // no bound on either side: no mask
     return d == 64 ? launch<64, fa::kMaskNone, false>(mq, mk, mv, mo, p, grid, stream)
                    : launch<128, fa::kMaskNone, false>(mq, mk, mv, mo, p, grid, stream);

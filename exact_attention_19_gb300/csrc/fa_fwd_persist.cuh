@@ -108,8 +108,10 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int x
 // One work unit as every role sees it.
 struct PUnit {
   int bh;
+  int j0;          // first K/V tile streamed (0 without a window)
   int row0[2];
-  int jhi[2];      // K/V tiles [0, jhi[t]) visible to query tile t (0 when the tile is absent)
+  int jlo[2];      // K/V tiles [j0 + jlo[t], j0 + jhi[t]) visible to query tile t;
+  int jhi[2];      // jlo = jhi = 0 when the tile is absent; jlo is 0 or 1
   int n_max;       // K/V tiles streamed: max(jhi)
 };
 
@@ -121,7 +123,7 @@ template <int D, int MASK>
 __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     fa_fwd_persist_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV, const FwdParams p, const int n_units) {
-  static_assert(MASK == kMaskNone || MASK == kMaskCausal, "no mask or causal");
+  static_assert(MASK == kMaskNone || MASK == kMaskCausal || MASK == kMaskWindow, "mask");
   constexpr bool kDynamic = MASK == kMaskCausal;
   using C = PCfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -193,15 +195,38 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
     }
     u.bh = bh;
     u.n_max = 0;
+    int lo[2], hi[2];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const int qt = 2 * pair + t;
       u.row0[t] = qt * C::kBM;
-      u.jhi[t] = 0;
-      if (u.row0[t] < p.Nq) u.jhi[t] = (MASK == kMaskCausal) ? min(n_kv, qt + 1) : n_kv;
+      lo[t] = 0;
+      hi[t] = 0;
+      if (u.row0[t] < p.Nq) {
+        hi[t] = (MASK == kMaskCausal) ? min(n_kv, qt + 1) : n_kv;
+        if (MASK == kMaskWindow) {
+          // a bounded band with Nq <= Nk: every row sees a key, and the two
+          // tiles' ranges are contiguous, tile 1's starting at most one later
+          const long long r_first = u.row0[t], r_last = min(u.row0[t] + C::kBM, p.Nq) - 1;
+          const long long key_lo = max(0ll, r_first + p.diag_off - p.win_left);
+          long long key_hi = p.Nk - 1;
+          if (p.win_right >= 0) key_hi = min(key_hi, r_last + p.diag_off + p.win_right);
+          lo[t] = static_cast<int>(key_lo / C::kBN);
+          hi[t] = static_cast<int>(key_hi / C::kBN) + 1;
+        }
+      }
+    }
+    u.j0 = lo[0];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      u.jlo[t] = hi[t] > lo[t] ? lo[t] - u.j0 : 0;
+      u.jhi[t] = hi[t] > lo[t] ? hi[t] - u.j0 : 0;
       u.n_max = max(u.n_max, u.jhi[t]);
     }
   };
+  // a unit's range start and first K/V tile: zero unless there is a window
+  auto lo_ = [](const PUnit& u, int t) -> int { return MASK == kMaskWindow ? u.jlo[t] : 0; };
+  auto j0_ = [](const PUnit& u) -> int { return MASK == kMaskWindow ? u.j0 : 0; };
   // Dynamic schedule: unit k >= 1 of this CTA is the answer to the k-th
   // cancellation request, in response slot (k - 1) % kUnitRing.
   auto resp_addr = [&](int s) -> uint32_t { return bar0 + kUnitRespOff + 16u * static_cast<uint32_t>(s); };
@@ -278,7 +303,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
           const CUtensorMap* map = (i & 1) ? &tmV : &tmK;
           mbar_arrive_expect_tx(full(s), C::kTileBytes);
           for (int b = 0; b < C::kBoxes; ++b)
-            tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (i >> 1) * C::kBN, u.bh);
+            tma_load_3d(slot_addr(s) + b * C::kBoxBytes, map, full(s), b * 64, (j0_(u) + (i >> 1)) * C::kBN, u.bh);
           issued = item + 1;
         }
         if (!ok) break;
@@ -399,7 +424,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         tc_fence_after();
         if (pv0) {
           ++np[0];
-          gemm2(0, sv, true);
+          gemm2(0, sv, jj > lo_(cur, 0));
           if (jj == cur.jhi[0] - 1) mma_commit_elect(bar(kPBarOFinal + 0));
         }
         if (jj + 1 < cur.jhi[0]) {
@@ -411,7 +436,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
           if (!uniform(mbar_wait(bar(kPBarP + 1), np[1] & 1, abort_flag))) return false;
           ++np[1];
           tc_fence_after();
-          gemm2(1, sv, true);
+          gemm2(1, sv, jj > lo_(cur, 1));
           if (jj == cur.jhi[1] - 1) mma_commit_elect(bar(kPBarOFinal + 1));
         }
         mma_commit_elect(empty(sv));
@@ -461,20 +486,29 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         const int iv = base_item + 2 * jj + 1, ik = iv + 1;
         const int sv = iv % C::kRing, sk = ik % C::kRing;
         const bool has_k = !last || has_nxt;
-        const bool pv0 = jj < cur.jhi[0], pv1 = jj < cur.jhi[1];
-        const bool sn0 = last ? (has_nxt && nxt.jhi[0] > 0) : (jj + 1 < cur.jhi[0]);
-        const bool sn1 = last ? (has_nxt && nxt.jhi[1] > 0) : (jj + 1 < cur.jhi[1]);
+        const bool pv0 = jj >= lo_(cur, 0) && jj < cur.jhi[0], pv1 = jj >= lo_(cur, 1) && jj < cur.jhi[1];
+        // the next unit's first S products: only for tiles whose range starts
+        // at its first K/V tile (a tile starting one later gets its first S
+        // in that unit's first step)
+        const bool sn0 = last ? (has_nxt && nxt.jhi[0] > 0 && lo_(nxt, 0) == 0) : (jj + 1 < cur.jhi[0]);
+        const bool sn1 = last ? (has_nxt && nxt.jhi[1] > 0 && lo_(nxt, 1) == 0) : (jj + 1 < cur.jhi[1]);
         if (!uniform(mbar_wait(full(sv), (iv / C::kRing) & 1, abort_flag))) return false;
         if (has_k && !uniform(mbar_wait(full(sk), (ik / C::kRing) & 1, abort_flag))) return false;
         if (pv0 && !uniform(mbar_wait(bar(kPBarP + 0), np[0] & 1, abort_flag))) return false;
         if (last) {
           if (sn0 && !uniform(mbar_wait(bar(kPBarQFull + 2 * qb_n[0] + 0), (occ_n[0] / C::kQBufs) & 1, abort_flag))) return false;
           if (sn1 && !uniform(mbar_wait(bar(kPBarQFull + 2 * qb_n[1] + 1), (occ_n[1] / C::kQBufs) & 1, abort_flag))) return false;
+        } else if (jj == 0) {
+          // a tile whose range starts one K/V tile late: its first S is issued here
+          if (sn0 && lo_(cur, 0) == 1 &&
+              !uniform(mbar_wait(bar(kPBarQFull + 2 * qb[0] + 0), (occ[0] / C::kQBufs) & 1, abort_flag))) return false;
+          if (sn1 && lo_(cur, 1) == 1 &&
+              !uniform(mbar_wait(bar(kPBarQFull + 2 * qb[1] + 1), (occ[1] / C::kQBufs) & 1, abort_flag))) return false;
         }
         tc_fence_after();
         if (pv0) {
           ++np[0];
-          gemm2(0, sv, jj > 0);
+          gemm2(0, sv, jj > lo_(cur, 0));
           if (jj == cur.jhi[0] - 1) mma_commit_elect(bar(kPBarOFinal + 0));
         }
         if (sn0) {
@@ -487,7 +521,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
           if (!uniform(mbar_wait(bar(kPBarP + 1), np[1] & 1, abort_flag))) return false;
           ++np[1];
           tc_fence_after();
-          gemm2(1, sv, jj > 0);
+          gemm2(1, sv, jj > lo_(cur, 1));
           if (jj == cur.jhi[1] - 1) mma_commit_elect(bar(kPBarOFinal + 1));
         }
         mma_commit_elect(empty(sv));
@@ -508,7 +542,7 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         if (ok) {
           tc_fence_after();
           for (int t = 0; t < 2; ++t)
-            if (cur.jhi[t] > 0) {
+            if (cur.jhi[t] > 0 && lo_(cur, t) == 0) {
               gemm1(t, qdesc(0, t), 0);
               mma_commit_elect(bar(kPBarS + t));
               if (cur.jhi[t] == 1) mma_commit_elect(bar(kPBarQFree + t));
@@ -530,11 +564,14 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
             dq_n[t] = qdesc(qb_n[t], t);
           }
           // steady range [1, s_hi): both tiles present, no last S or P V of either
+          // (and past both tiles' first P V)
+          const int s_lo = max(lo_(cur, 0), lo_(cur, 1)) + 1;
           int s_hi = 1;
           if (cur.jhi[1] > 0) s_hi = max(1, min(cur.jhi[0], cur.jhi[1]) - 2);
           const int n = cur.n_max;
           ok = boundary(0);
           int jj = 1;
+          for (; ok && jj < s_lo && jj < n - 1; ++jj) ok = inner(jj);
           for (; ok && jj < s_hi && jj < n - 1; ++jj) ok = steady(jj);
           for (; ok && jj < n - 1; ++jj) ok = inner(jj);
           if (ok && n > 1) ok = boundary(n - 1);
@@ -573,11 +610,19 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         break;
       }
       if (r == 0) break;
-      const int nt = u.jhi[t];
+      const int nt = u.jhi[t] - lo_(u, t);
       if (nt == 0) continue;
       const int row = u.row0[t] + row_local;
-      // keys past Nk (the ragged last tile) and, causal, past the row are masked
-      const int row_key_end = (MASK == kMaskCausal) ? min(p.Nk, row + 1) : p.Nk;
+      const int key0 = (j0_(u) + lo_(u, t)) * C::kBN;  // first key of the tile's first K/V tile
+      // keys past Nk (the ragged last tile), causal past the row, and outside
+      // a window's band are masked
+      int row_key_lo = 0, row_key_end = (MASK == kMaskCausal) ? min(p.Nk, row + 1) : p.Nk;
+      if (MASK == kMaskWindow) {
+        row_key_lo = static_cast<int>(max(-1ll, static_cast<long long>(row) + p.diag_off - p.win_left));
+        if (p.win_right >= 0)
+          row_key_end = static_cast<int>(
+              min(static_cast<long long>(p.Nk), max(-1ll, static_cast<long long>(row) + p.diag_off + p.win_right) + 1));
+      }
       float m_bar = NEG_INF;  // reference maximum, base-2 scaled units
       float l = 0.f;
       float r_max = NEG_INF;  // the row's largest score (raw units); see fa_fwd_kernel
@@ -601,14 +646,15 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         float* const f1 = reinterpret_cast<float*>(s1);
         float* const f2 = reinterpret_cast<float*>(s2);
         float* const f3 = reinterpret_cast<float*>(s3);
-        const int k0 = j * C::kBN;
+        const int k0 = key0 + j * C::kBN;
+        const int lim_lo = MASK == kMaskWindow ? min(C::kBN, max(0, row_key_lo - k0)) : 0;
         const int lim_hi = min(C::kBN, max(0, row_key_end - k0));
-        const bool masked = lim_hi < C::kBN;
+        const bool masked = lim_lo > 0 || lim_hi < C::kBN;
         if (masked) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if (i >= lim_hi) f0[i] = NEG_INF;
-            if (32 + i >= lim_hi) f1[i] = NEG_INF;
+            if (i < lim_lo || i >= lim_hi) f0[i] = NEG_INF;
+            if (32 + i < lim_lo || 32 + i >= lim_hi) f1[i] = NEG_INF;
           }
         }
         float mx0 = fmax3(f0[0], f0[1], f1[0]), mx1 = fmax3(f0[2], f0[3], f1[1]);
@@ -624,8 +670,8 @@ __global__ void __launch_bounds__(PCfg<D>::kThreads, 1)
         if (masked) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            if (64 + i >= lim_hi) f2[i] = NEG_INF;
-            if (96 + i >= lim_hi) f3[i] = NEG_INF;
+            if (64 + i < lim_lo || 64 + i >= lim_hi) f2[i] = NEG_INF;
+            if (96 + i < lim_lo || 96 + i >= lim_hi) f3[i] = NEG_INF;
           }
         }
         float mx2 = fmax3(f2[0], f2[1], f3[0]), mx3 = fmax3(f2[2], f2[3], f3[1]);

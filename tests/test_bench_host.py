@@ -64,7 +64,9 @@ def test_kernel_name_follows_dispatch():
     assert bench.kernel_name(synth.WORKLOADS["long_8192_d64"].with_(causal=True), None) == "fa_fwd_persist_kernel"
     few = synth.WORKLOADS["long_8192_d64"].with_(causal=True, B=1, H=8)  # 256 pairs: under 6 per SM
     assert bench.kernel_name(few, None) == "fa_fwd_kernel"
-    assert bench.kernel_name(w.with_(window=(64, 0)), None) == "fa_fwd_kernel"
+    assert bench.kernel_name(w.with_(window=(64, 0)), None) == "fa_fwd_persist_kernel"
+    assert bench.kernel_name(w.with_(window=(64, -1)), None) == "fa_fwd_kernel"
+    assert bench.kernel_name(w.with_(window=(64, 0), B=1, H=8), None) == "fa_fwd_kernel"
 
 
 def test_causal_flag_rejects_window():

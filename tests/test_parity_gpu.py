@@ -389,6 +389,21 @@ def test_window_parity(nq, nk, window, d):
     _assert_close_window(o, lse, o_ref, lse_ref, f"window {window} {nq}x{nk} d{d}")
 
 
+# a window bounded on both sides with Nq <= Nk and at least 4 query-tile pairs
+# per SM: the persistent kernel (tile 1's range may start one K/V tile after
+# tile 0's; both are masked at both ends)
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("window", [(200, 50), (0, 0), (127, 128), (1000, 1000), (5, 300)])
+@pytest.mark.parametrize("shape", [(4, 64, 700, 700), (4, 80, 300, 1000)])
+def test_window_persistent(shape, window, d):
+    B, H, nq, nk = shape
+    w = synth.Workload("winp", B, H, nq, nk, d, False, seed=71 + nq + nk + d)
+    q, k, v = w.make()
+    o, lse = _run_window(q, k, v, w.scale, window)
+    o_ref, lse_ref = oracle.attention_fwd(q, k, v, w.scale, window=window)
+    _assert_close_window(o, lse, o_ref, lse_ref, f"window {window} {B}x{H}x{nq}x{nk} d{d}")
+
+
 def test_window_equal_to_causal_when_square():
     w = synth.Workload("wc", 1, 3, 1000, 1000, 128, True, seed=62)
     q, k, v = w.make()
