@@ -689,7 +689,8 @@ def main(argv=None):
             ap.error("--window takes two integers: LEFT,RIGHT")
         if wl < -1 or wr < -1:
             ap.error("--window bounds must be >= -1")
-        w = w.with_(window=(wl, wr), causal=False)
+        # its own name: the window's launch has its own DRAM traffic (and config)
+        w = w.with_(window=(wl, wr), causal=False, name=f"{w.name}_window_{wl}_{wr}")
     if args.causal:
         if args.window is not None:
             ap.error("--causal and --window exclude each other")
